@@ -1,0 +1,217 @@
+"""WISE block-sparse causal attention on GB300 (sm_103a).
+
+Python front end of the C-ABI library ``libwise.so``. The three calls follow
+"Attention Routing Stabilizes Early: Working-Set Inference for Recurrent
+Language Models" (WISE):
+
+* :func:`discover`        -- early recurrent step: unrestricted causal
+  attention (§3 Eq 2) plus the block masses r_qb (§5.1 Eq 5);
+* :func:`select_support`  -- once after discovery: the cumulative-mass block
+  support of §5.1 Eq 6, unioned over the discovery window, as a CSR;
+* :func:`sparse`          -- late recurrent step: attention over the reused
+  support only (§5.2 Eqs 7-8).
+
+Torch tensors supply device memory and the stream; every computation runs in
+the library's CUDA kernels. There is no CPU path: without the compiled
+library on a CUDA device these functions raise.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import (WISE_BF16, WISE_F32, WISE_SUPPORT_DIAG, WISE_SUPPORT_SINK, WiseError)  # noqa: F401
+
+__all__ = ["discover", "select_support", "sparse", "Support", "device_status", "WiseError",
+           "WISE_SUPPORT_SINK", "WISE_SUPPORT_DIAG", "useful_flops", "dense_flops"]
+
+_OUT = {torch.bfloat16: WISE_BF16, torch.float32: WISE_F32}
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> None:
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+        if not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous [batch, heads, seq, head_dim] tensor")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must have the same shape")
+
+
+def _desc(shape: Sequence[int], block: int, scale: float, out_dtype: torch.dtype) -> _lib.AttnDesc:
+    b, h, n, d = shape
+    if out_dtype not in _OUT:
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
+    return _lib.make_desc(b, h, n, d, block, scale, _OUT[out_dtype])
+
+
+def discover_workspace_bytes(shape: Sequence[int], block: int) -> int:
+    d = _desc(shape, block, 0.0, torch.bfloat16)
+    return int(_lib.load().wise_attn_discover_workspace(d))
+
+
+def discover(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: int, *, want_mass: bool = True,
+             want_lse: bool = True, out_dtype: torch.dtype = torch.bfloat16, scale: float = 0.0,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             mass: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None):
+    """Discovery step. Returns (O, LSE or None, block masses [B,H,nb,nb] or None)."""
+    _check_qkv(q, k, v)
+    lib = _lib.load()
+    b, h, n, d = q.shape
+    desc = _desc(q.shape, block, scale, out_dtype)
+    if out is None:
+        out = torch.empty((b, h, n, d), dtype=out_dtype, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    nb = n // block if block > 0 else 0
+    ws_bytes = 0
+    if want_mass:
+        if mass is None:
+            mass = torch.empty((b, h, nb, nb), dtype=torch.float32, device=q.device)
+        ws_bytes = int(lib.wise_attn_discover_workspace(desc))
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    else:
+        mass = None
+    st = lib.wise_attn_discover(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), _ptr(lse),
+                                _ptr(mass), _ptr(workspace) if want_mass else None,
+                                workspace.numel() if (want_mass and workspace is not None) else 0,
+                                _stream_handle(stream))
+    _lib.check(st, "wise_attn_discover")
+    return out, (lse if want_lse else None), mass
+
+
+@dataclasses.dataclass
+class Support:
+    """The reused working set: CSR over rows (batch, head, query block)."""
+    row_ptr: torch.Tensor      # int32 [B*H*nb + 1]
+    col_idx: torch.Tensor      # int32 [capacity]
+    tile_order: torch.Tensor   # int32 [units]: late-step work order
+    nnz: torch.Tensor          # int32 [1] (device)
+    batch: int
+    heads: int
+    seq_len: int
+    head_dim: int
+    block: int
+
+    @property
+    def n_blocks(self) -> int:
+        return self.seq_len // self.block
+
+    def to_lists(self):
+        rp = self.row_ptr.cpu().numpy()
+        ci = self.col_idx.cpu().numpy()
+        return [ci[rp[r]:rp[r + 1]].tolist() for r in range(len(rp) - 1)]
+
+
+def select_support(masses: torch.Tensor, seq_len: int, head_dim: int, block: int, eta: float,
+                   flags: int = WISE_SUPPORT_SINK | WISE_SUPPORT_DIAG, *,
+                   support: Optional[Support] = None, workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> Support:
+    """Working-set selection from the window's masses [W, B, H, nb, nb] (f32)."""
+    if not masses.is_cuda or masses.dtype != torch.float32 or masses.dim() != 5 or not masses.is_contiguous():
+        raise ValueError("masses must be a contiguous float32 CUDA tensor [W, B, H, nb, nb]")
+    lib = _lib.load()
+    w, b, h, nb, nb2 = masses.shape
+    if nb != nb2 or nb * block != seq_len:
+        raise ValueError("mass shape does not match seq_len / block")
+    desc = _lib.make_desc(b, h, seq_len, head_dim, block)
+    cap = int(lib.wise_support_capacity(desc))
+    units = int(lib.wise_schedule_units(desc))
+    dev = masses.device
+    if support is None:
+        support = Support(torch.empty(b * h * nb + 1, dtype=torch.int32, device=dev),
+                          torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+                          torch.empty(max(units, 1), dtype=torch.int32, device=dev),
+                          torch.empty(1, dtype=torch.int32, device=dev), b, h, seq_len, head_dim, block)
+    ws_bytes = int(lib.wise_select_workspace(desc, w))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    st = lib.wise_select_support(desc, masses.data_ptr(), w, float(eta), flags, support.row_ptr.data_ptr(),
+                                 support.col_idx.data_ptr(), support.col_idx.numel(),
+                                 support.tile_order.data_ptr(), support.nnz.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel(), _stream_handle(stream))
+    _lib.check(st, "wise_select_support")
+    return support
+
+
+def sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, support: Support, *, want_lse: bool = True,
+           out_dtype: torch.dtype = torch.bfloat16, scale: float = 0.0, out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None, use_schedule: bool = True,
+           stream: Optional[torch.cuda.Stream] = None):
+    """Late (reuse) step over the support. Returns (O, LSE or None)."""
+    _check_qkv(q, k, v)
+    lib = _lib.load()
+    b, h, n, d = q.shape
+    if (b, h, n, d) != (support.batch, support.heads, support.seq_len, support.head_dim):
+        raise ValueError("support was built for a different shape")
+    desc = _desc(q.shape, support.block, scale, out_dtype)
+    if out is None:
+        out = torch.empty((b, h, n, d), dtype=out_dtype, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    st = lib.wise_attn_sparse(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), support.row_ptr.data_ptr(),
+                              support.col_idx.data_ptr(), support.col_idx.numel(),
+                              support.tile_order.data_ptr() if use_schedule else None, out.data_ptr(),
+                              _ptr(lse) if want_lse else None, _stream_handle(stream))
+    _lib.check(st, "wise_attn_sparse")
+    return out, (lse if want_lse else None)
+
+
+def support_from_lists(rows, batch: int, heads: int, seq_len: int, head_dim: int, block: int,
+                       device="cuda") -> Support:
+    """A Support from explicit ascending key-block lists (rows ordered batch,
+    head, query block); tile_order is left to the kernel's natural order."""
+    lib = _lib.load()
+    rp = [0]
+    cols = []
+    for r in rows:
+        cols.extend(int(x) for x in r)
+        rp.append(len(cols))
+    desc = _lib.make_desc(batch, heads, seq_len, head_dim, block)
+    units = int(lib.wise_schedule_units(desc))
+    return Support(torch.tensor(rp, dtype=torch.int32, device=device),
+                   torch.tensor(cols if cols else [0], dtype=torch.int32, device=device),
+                   torch.zeros(max(units, 1), dtype=torch.int32, device=device),
+                   torch.tensor([len(cols)], dtype=torch.int32, device=device),
+                   batch, heads, seq_len, head_dim, block)
+
+
+def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise and read/clear the library's device error word."""
+    return int(_lib.load().wise_device_status(_stream_handle(stream)))
+
+
+def check_device(stream: Optional[torch.cuda.Stream] = None) -> None:
+    _lib.check(device_status(stream), "device")
+
+
+# ---------------------------------------------------------------- FLOP counts
+
+def dense_flops(batch: int, heads: int, seq_len: int, head_dim: int) -> float:
+    """Useful FLOPs of causal attention: 4 d per admissible (i, j) pair."""
+    return 4.0 * head_dim * batch * heads * seq_len * (seq_len + 1) / 2
+
+
+def useful_flops(rows_per_bh_counts, block: int, head_dim: int) -> float:
+    """Useful FLOPs over a block support: 4 d per admissible pair inside the
+    listed blocks (B^2 off the diagonal, B(B+1)/2 on it). `rows_per_bh_counts`
+    is a pair (n_offdiag_blocks, n_diag_blocks)."""
+    off, diag = rows_per_bh_counts
+    return 4.0 * head_dim * (off * block * block + diag * block * (block + 1) / 2)

@@ -1,0 +1,574 @@
+// Causal flash attention on sm_103a tensor cores (tcgen05 + TMEM + TMA), used
+// for both WISE steps that touch Q/K/V:
+//
+//  * discover (SPARSE = false): unrestricted causal attention, §3 Eq 2 of
+//    "Attention Routing Stabilizes Early: Working-Set Inference for Recurrent
+//    Language Models" (WISE), optionally with the §5.1 Eq 5 block masses;
+//  * reuse    (SPARSE = true): attention restricted to the CSR block support,
+//    §5.2 Eqs 7-8 -- only listed key blocks are loaded and multiplied.
+//
+// One CTA = one work unit = two 128-row query tiles ("streams") of one
+// (batch, head). Warp roles (320 threads):
+//   warp 0      TMA producer: Q tiles once, then K/V blocks into an NST ring
+//   warp 1      TMEM allocator + MMA issuer (single thread)
+//   warps 2-5   softmax warpgroup of stream 0 (one query row per thread)
+//   warps 6-9   softmax warpgroup of stream 1
+// The MMA thread walks the ascending union of both streams' key-block lists;
+// a K/V block read by both streams is loaded once. Per stream, S = Q K^T goes
+// to its own TMEM columns; the softmax warps turn S into P (bf16, written
+// back over S) and the MMA thread accumulates O += P V from TMEM. While one
+// stream's warps run the softmax, the tensor core works on the other stream.
+// The running row max is only moved (and O rescaled) when it grows by more
+// than 2^8, so most tiles skip the O correction.
+#pragma once
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace wise {
+
+template <int D, int BN>
+struct AttnCfg {
+  static_assert(D == 64 || D == 96 || D == 128, "head_dim");
+  static_assert(BN == 64 || BN == 128, "block");
+  static constexpr int CH = (D == 96) ? 32 : 64;         // elements per swizzled smem row
+  static constexpr int NCH = D / CH;                     // TMA boxes per tile
+  static constexpr uint32_t SWZ = (CH == 64) ? 2u : 4u;  // descriptor code: 128B / 64B swizzle
+  static constexpr uint32_t ROWB = CH * 2;               // bytes per swizzled row
+  static constexpr uint32_t Q_BYTES = 128u * D * 2u;
+  static constexpr uint32_t KV_BYTES = (uint32_t)BN * D * 2u;
+  static constexpr uint32_t SMEM_BUDGET = 230400u;
+  static constexpr int NST_FIT = (int)((SMEM_BUDGET - 2u * Q_BYTES) / (2u * KV_BYTES));
+  static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;  // K/V ring depth
+  static_assert(NST >= 2, "ring");
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = 2u * Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + NST * KV_BYTES;
+  // q_full[2] k_full[NST] v_full[NST] kv_empty[NST] s_full[2] p_full[2] o_final[2] drain
+  static constexpr int NBAR = 2 + 3 * NST + 2 + 2 + 2 + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16u + 1024u;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM columns: S/P of stream i at s_col(i), O of stream i at o_col(i)
+  __host__ __device__ static constexpr uint32_t s_col(int i) { return i ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t o_col(int i) { return i ? 384u : 256u; }
+  static constexpr int ENT_PER_TILE = 128 / BN;  // key blocks per 128 rows
+};
+
+// Entries (key blocks) of one 128-row query tile in ascending order. Dense:
+// the causal range. Sparse: the union of the CSR lists of the query blocks
+// inside the tile (one for BN = 128, two for BN = 64); bit j of `mask` says
+// whether query block j of the tile lists the entry. List values that are not
+// strictly ascending or not admissible (b > q) are skipped and reported.
+struct TileCursor {
+  const int32_t* col;
+  int32_t pos[2], end[2], last[2], maxv[2];
+  int32_t head[2];
+  int32_t next_dense, dense_end;
+  bool sparse, bad;
+
+  __device__ __forceinline__ int32_t adv(int j) {
+    while (pos[j] < end[j]) {
+      const int32_t v = __ldg(col + pos[j]);
+      ++pos[j];
+      if (v > last[j] && v <= maxv[j]) {
+        last[j] = v;
+        return v;
+      }
+      bad = true;
+    }
+    return INT32_MAX;
+  }
+
+  __device__ __forceinline__ void init_empty() {
+    sparse = false;
+    next_dense = 0;
+    dense_end = 0;
+    bad = false;
+  }
+  __device__ __forceinline__ void init_dense(int t, const AttnParams& p, int bn) {
+    sparse = false;
+    bad = false;
+    next_dense = 0;
+    const int rows_end = min(128 * (t + 1), p.n);
+    dense_end = (rows_end - 1) / bn + 1;
+  }
+  __device__ __forceinline__ void init_sparse(int t, int bh, const AttnParams& p, int ent_per_tile) {
+    sparse = true;
+    bad = false;
+    col = p.col_idx;
+    for (int j = 0; j < 2; ++j) {
+      pos[j] = end[j] = 0;
+      last[j] = -1;
+      maxv[j] = -1;
+      const int qb = t * ent_per_tile + j;
+      if (j < ent_per_tile && qb < p.nb) {
+        const int64_t r = (int64_t)bh * p.nb + qb;
+        const int32_t a = __ldg(p.row_ptr + r), b = __ldg(p.row_ptr + r + 1);
+        if (a >= 0 && a <= b && (int64_t)b <= p.col_cap) {
+          pos[j] = a;
+          end[j] = b;
+          maxv[j] = qb;
+        } else {
+          bad = true;
+        }
+      }
+    }
+    head[0] = adv(0);
+    head[1] = adv(1);
+  }
+  __device__ __forceinline__ bool next(int32_t& blk, uint32_t& mask) {
+    if (!sparse) {
+      if (next_dense >= dense_end) return false;
+      blk = next_dense++;
+      mask = 3u;
+      return true;
+    }
+    if (head[0] == INT32_MAX && head[1] == INT32_MAX) return false;
+    blk = min(head[0], head[1]);
+    mask = (head[0] == blk ? 1u : 0u) | (head[1] == blk ? 2u : 0u);
+    if (head[0] == blk) head[0] = adv(0);
+    if (head[1] == blk) head[1] = adv(1);
+    return true;
+  }
+};
+
+// Ascending union of the two streams' entries; `who` bit i = stream i uses it.
+struct PairCursor {
+  TileCursor c[2];
+  int32_t head[2];
+  __device__ __forceinline__ void start() {
+    uint32_t m;
+    for (int i = 0; i < 2; ++i)
+      if (!c[i].next(head[i], m)) head[i] = INT32_MAX;
+  }
+  __device__ __forceinline__ bool next(int32_t& blk, uint32_t& who) {
+    if (head[0] == INT32_MAX && head[1] == INT32_MAX) return false;
+    blk = min(head[0], head[1]);
+    who = (head[0] == blk ? 1u : 0u) | (head[1] == blk ? 2u : 0u);
+    uint32_t m;
+    for (int i = 0; i < 2; ++i)
+      if (head[i] == blk && !c[i].next(head[i], m)) head[i] = INT32_MAX;
+    return true;
+  }
+};
+
+// Default order of work units: (batch, head) slices in groups sized so the
+// group's K/V stays in L2, heavier (later) query tiles first inside a group.
+__device__ __forceinline__ int64_t default_unit(int64_t x, const AttnParams& p) {
+  const int64_t g_heads = p.group_heads;
+  const int64_t per_group = g_heads * p.npairs;
+  const int64_t g = x / per_group, w = x % per_group;
+  const int64_t gsize = min(g_heads, (int64_t)p.bh_count - g * g_heads);
+  const int64_t pr = p.npairs - 1 - w / gsize;
+  const int64_t bh = g * g_heads + w % gsize;
+  return bh * p.npairs + pr;
+}
+
+__device__ __forceinline__ int64_t lam_tile_offset(int bh, int t, const AttnParams& p, int ept) {
+  const int64_t before = (int64_t)ept * t * (t + 1) / 2;
+  const int64_t total = (int64_t)ept * p.n_qtiles * (p.n_qtiles + 1) / 2;
+  return ((int64_t)bh * total + before) * 128;
+}
+
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  int dummy_abort = 0;
+  return mbar_wait(bar, parity, &dummy_abort, err);
+}
+
+template <int D, int BN, bool SPARSE>
+__global__ void __launch_bounds__(320, 1)
+    wise_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  using C = AttnCfg<D, BN>;
+  constexpr int NST = C::NST;
+  constexpr uint32_t ROWB = C::ROWB;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ[2] = {smem + C::OFF_Q, smem + C::OFF_Q + C::Q_BYTES};
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 2;
+  uint64_t* v_full = k_full + NST;
+  uint64_t* kv_empty = v_full + NST;
+  uint64_t* s_full = kv_empty + NST;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_final = p_full + 2;
+  uint64_t* drain = o_final + 2;
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  int64_t unit;
+  if (SPARSE && p.tile_order != nullptr) {
+    unit = __ldg(p.tile_order + blockIdx.x);
+  } else {
+    unit = default_unit(blockIdx.x, p);
+  }
+  if (unit < 0 || unit >= p.n_units) {  // malformed schedule: whole CTA leaves before any setup
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadSupport);
+    return;
+  }
+  const int bh = (int)(unit / p.npairs);
+  const int pair = (int)(unit % p.npairs);
+  const int tile[2] = {2 * pair, 2 * pair + 1};
+  const bool has1 = tile[1] < p.n_qtiles;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full[0], 1);
+    mbar_init(&q_full[1], 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_final[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_base_slot;
+
+  auto make_cursor = [&](TileCursor& c, int i) {
+    if (i == 1 && !has1) {
+      c.init_empty();
+    } else if (SPARSE) {
+      c.init_sparse(tile[i], bh, p, C::ENT_PER_TILE);
+    } else {
+      c.init_dense(tile[i], p, BN);
+    }
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int i = 0; i < (has1 ? 2 : 1); ++i) {
+        const int row = bh * p.n + tile[i] * 128;
+        mbar_arrive_expect_tx(&q_full[i], C::Q_BYTES);
+        for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ[i] + c * 128 * ROWB, &tm_q, &q_full[i], c * C::CH, row);
+      }
+      PairCursor pc;
+      make_cursor(pc.c[0], 0);
+      make_cursor(pc.c[1], 1);
+      if (pc.c[0].bad || pc.c[1].bad) atomicOr(p.err, kErrBadSupport);
+      pc.start();
+      int k = 0;
+      int32_t blk;
+      uint32_t who;
+      while (pc.next(blk, who)) {
+        const int s = k % NST;
+        if (k >= NST && !mbar_wait(&kv_empty[s], ((k / NST) - 1) & 1, abort_flag, p.err)) break;
+        const int row = bh * p.n + blk * BN;
+        uint8_t* sk = smem + C::OFF_K + s * C::KV_BYTES;
+        uint8_t* sv = smem + C::OFF_V + s * C::KV_BYTES;
+        mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
+        for (int c = 0; c < C::NCH; ++c) tma_load_2d(sk + c * BN * ROWB, &tm_k, &k_full[s], c * C::CH, row);
+        mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
+        for (int c = 0; c < C::NCH; ++c) tma_load_2d(sv + c * BN * ROWB, &tm_v, &v_full[s], c * C::CH, row);
+        ++k;
+      }
+      if (pc.c[0].bad || pc.c[1].bad) atomicOr(p.err, kErrBadSupport);
+      // No copy into this CTA's shared memory may outlive the CTA.
+      for (int j = (k > NST ? k - NST : 0); j < k; ++j) {
+        const int s = j % NST;
+        const uint32_t ph = (j / NST) & 1;
+        mbar_wait_drain(&k_full[s], ph, p.err);
+        mbar_wait_drain(&v_full[s], ph, p.err);
+      }
+      mbar_wait_drain(&q_full[0], 0, p.err);
+      if (has1) mbar_wait_drain(&q_full[1], 0, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
+      PairCursor pc;
+      make_cursor(pc.c[0], 0);
+      make_cursor(pc.c[1], 1);
+      pc.start();
+      bool ok = true;
+      bool q_ready[2] = {false, false};
+      bool pending[2] = {false, false};
+      int pend_slot[2] = {0, 0};
+      uint32_t pend_ph[2] = {0, 0};
+      uint32_t n_pv[2] = {0, 0};
+      uint32_t rem[NST];
+      for (int s = 0; s < NST; ++s) rem[s] = 0;
+
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(&p_full[i], n_pv[i] & 1, abort_flag, p.err)) return false;
+        const int s = pend_slot[i];
+        if (!mbar_wait(&v_full[s], pend_ph[i], abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t vbase = smem_u32(smem + C::OFF_V + s * C::KV_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bdesc = smem_desc(vbase + kk * 16 * ROWB, BN * ROWB, 8 * ROWB, C::SWZ);
+          umma_ts(tbase + C::o_col(i), tbase + C::s_col(i) + kk * 8, bdesc, IDESC_O, (n_pv[i] | kk) != 0);
+        }
+        ++n_pv[i];
+        if (--rem[s] == 0) umma_commit(&kv_empty[s]);
+        pending[i] = false;
+        return true;
+      };
+
+      int k = 0;
+      int32_t blk;
+      uint32_t who;
+      while (ok && pc.next(blk, who)) {
+        const int s = k % NST;
+        const uint32_t ph = (k / NST) & 1;
+        bool k_ready = false;
+        rem[s] = __popc(who);
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (pending[i] && !(ok = issue_pv(i))) break;
+          if (!(who & (1u << i))) continue;
+          if (!q_ready[i]) {
+            if (!(ok = mbar_wait(&q_full[i], 0, abort_flag, p.err))) break;
+            q_ready[i] = true;
+          }
+          if (!k_ready) {
+            if (!(ok = mbar_wait(&k_full[s], ph, abort_flag, p.err))) break;
+            k_ready = true;
+          }
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sQ[i]);
+          const uint32_t ka = smem_u32(smem + C::OFF_K + s * C::KV_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int c = kk / (C::CH / 16), w = kk % (C::CH / 16);
+            const uint64_t adesc = smem_desc(qa + c * 128 * ROWB + w * 32, 16, 8 * ROWB, C::SWZ);
+            const uint64_t bdesc = smem_desc(ka + c * BN * ROWB + w * 32, 16, 8 * ROWB, C::SWZ);
+            umma_ss(tbase + C::s_col(i), adesc, bdesc, IDESC_S, kk > 0);
+          }
+          umma_commit(&s_full[i]);
+          pending[i] = true;
+          pend_slot[i] = s;
+          pend_ph[i] = ph;
+        }
+        ++k;
+      }
+      for (int i = 0; i < 2 && ok; ++i)
+        if (pending[i]) ok = issue_pv(i);
+      for (int i = 0; i < 2; ++i)
+        if (n_pv[i] > 0) umma_commit(&o_final[i]);
+      umma_commit(drain);  // every MMA of this CTA done before TMEM is released
+      mbar_wait_drain(drain, 0, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int i = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
+    if (!(i == 1 && !has1)) {
+      const int t = tile[i];
+      const int qpos = t * 128 + r;
+      const bool row_valid = qpos < p.n;
+      const uint32_t trow = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t tS = trow + C::s_col(i);
+      const uint32_t tO = trow + C::o_col(i);
+      const float sl2 = p.scale_log2;
+      const bool want_mass = (!SPARSE) && (p.mass != nullptr);
+      float* lam = want_mass ? p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + r : nullptr;
+      const int half = (BN == 64) ? (r >> 6) : 0;
+
+      TileCursor cur;
+      make_cursor(cur, i);
+      float m_ref = -INFINITY, l = 0.f;
+      uint32_t cnt = 0;
+      bool ok = true;
+      int32_t blk;
+      uint32_t mask;
+      while (cur.next(blk, mask)) {
+        ok = mbar_wait(&s_full[i], cnt & 1, abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int kbase = blk * BN;
+        const bool row_on = (mask >> half) & 1u;
+        // columns c <= limit are admissible (causal mask M, working-set mask R)
+        const int limit = row_on ? ((kbase + BN - 1 > qpos) ? qpos - kbase : BN) : -1;
+        const bool full = limit >= BN - 1;
+        // pass 1: row max, 64 columns at a time (keeps register use low)
+        float mx = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t s[2][32];
+          tmem_ld_x32(tS + h * 64, s[0]);
+          tmem_ld_x32(tS + h * 64 + 32, s[1]);
+          tmem_wait_ld(s[0]);
+          tmem_wait_ld(s[1]);
+          if (full) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+              for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(s[cc][j]));
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                mx = fmaxf(mx, (h * 64 + cc * 32 + j <= limit) ? __uint_as_float(s[cc][j]) : -INFINITY);
+          }
+        }
+        mx *= sl2;
+        float factor = 1.f;
+        bool resc = false;
+        if (cnt == 0) {
+          m_ref = mx;
+        } else if (mx > m_ref + 8.f) {
+          factor = fast_exp2(m_ref - mx);
+          m_ref = mx;
+          resc = true;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, written over S
+        float rs = 0.f;
+#pragma unroll
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t s[2][32];
+          tmem_ld_x32(tS + h * 64, s[0]);
+          tmem_ld_x32(tS + h * 64 + 32, s[1]);
+          tmem_wait_ld(s[0]);
+          tmem_wait_ld(s[1]);
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int cc = j >> 4, jj = (j & 15) * 2;
+            const int c0 = h * 64 + 2 * j;
+            float p0 = fast_exp2(fmaf(__uint_as_float(s[cc][jj]), sl2, -m_use));
+            float p1 = fast_exp2(fmaf(__uint_as_float(s[cc][jj + 1]), sl2, -m_use));
+            if (!full) {
+              p0 = (c0 <= limit) ? p0 : 0.f;
+              p1 = (c0 + 1 <= limit) ? p1 : 0.f;
+            }
+            rs += p0 + p1;
+            pk[j] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_x32(tS + h * 32, pk);
+        }
+        l = l * factor + rs;
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + cc * 32, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
+            tmem_st_x32(tO + cc * 32, o);
+          }
+        }
+        tmem_wait_st();
+        if (want_mass) lam[(size_t)cnt * 128] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
+        tc_fence_before();
+        mbar_arrive(&p_full[i]);
+        ++cnt;
+      }
+
+      // ------------------------------------------------------------ epilogue
+      if (ok && cnt > 0) {
+        ok = mbar_wait(&o_final[i], 0, abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+      }
+      if (ok) {
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const size_t grow = (size_t)bh * p.n + qpos;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          if (cnt > 0) {
+            tmem_ld_x32(tO + cc * 32, o);
+            tmem_wait_ld(o);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = 0u;
+          }
+          if (row_valid) {
+            if (p.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + grow * D + cc * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv_l, __uint_as_float(o[4 * j + 1]) * inv_l,
+                                     __uint_as_float(o[4 * j + 2]) * inv_l, __uint_as_float(o[4 * j + 3]) * inv_l);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D + cc * 32);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(o[8 * j + 0]) * inv_l, __uint_as_float(o[8 * j + 1]) * inv_l);
+                v.y = pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv_l, __uint_as_float(o[8 * j + 3]) * inv_l);
+                v.z = pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv_l, __uint_as_float(o[8 * j + 5]) * inv_l);
+                v.w = pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv_l, __uint_as_float(o[8 * j + 7]) * inv_l);
+                dst[j] = v;
+              }
+            }
+          }
+        }
+        const float lse2 = (l > 0.f) ? m_use + fast_log2(l) : -INFINITY;
+        if (p.lse != nullptr && row_valid) p.lse[grow] = lse2 * 0.69314718055994531f;
+        if (want_mass) {
+          // Eq 5: r_qb = (1/B) sum over the block's rows of 2^(lam_ib - lse2_i).
+          float* part = reinterpret_cast<float*>(sQ[i]);  // Q tile is dead once o_final fired
+#pragma unroll 1
+          for (uint32_t e = 0; e < cnt; ++e) {
+            float a = (row_valid && l > 0.f) ? fast_exp2(lam[(size_t)e * 128] - lse2) : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+            if (lane == 0) part[quarter * p.nb + e] = a;
+          }
+          named_bar_sync(1 + i, 128);
+          constexpr int QB_PER_TILE = C::ENT_PER_TILE;
+          for (int qq = 0; qq < QB_PER_TILE; ++qq) {
+            const int qb = t * QB_PER_TILE + qq;
+            if (qb >= p.nb) break;
+            float* dst = p.mass + ((size_t)bh * p.nb + qb) * p.nb;
+            for (int e = r; e < p.nb; e += 128) {
+              float v = 0.f;
+              if (e < (int)cnt) {
+                if (BN == 128) {
+                  v = (part[0 * p.nb + e] + part[1 * p.nb + e]) + (part[2 * p.nb + e] + part[3 * p.nb + e]);
+                } else {
+                  v = part[(2 * qq) * p.nb + e] + part[(2 * qq + 1) * p.nb + e];
+                }
+                v *= (1.f / BN);
+              }
+              dst[e] = v;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+}  // namespace wise

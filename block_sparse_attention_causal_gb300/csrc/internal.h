@@ -1,0 +1,54 @@
+// Internal host/device interfaces shared by the translation units of libwise.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace wise {
+
+struct AttnParams {
+  int32_t bh_count;     // batch * heads
+  int32_t n;            // sequence length
+  int32_t nb;           // n / BN key (and query) blocks
+  int32_t n_qtiles;     // ceil(n / 128)
+  int32_t npairs;       // ceil(n_qtiles / 2): work units per (batch, head)
+  int32_t group_heads;  // (batch, head) slices per L2 group in the default order
+  float scale_log2;     // softmax scale * log2(e)
+  int32_t out_f32;      // O dtype: 0 bf16, 1 f32
+  void* o;
+  float* lse;           // optional
+  float* mass;          // optional [bh, nb, nb] (discover only)
+  float* lam;           // per-row per-entry log2-sum-exp scratch (mass only)
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  int64_t col_cap;
+  const int32_t* tile_order;  // optional unit order (reuse only)
+  int64_t n_units;
+  uint32_t* err;
+};
+
+struct SelectLaunch {
+  const float* mass;
+  int32_t window, bh_count, nb;
+  int64_t target_fx, tol_fx;
+  uint32_t flags;
+  uint32_t* bits;
+  int32_t* counts;
+  int32_t* row_ptr;
+  int32_t* col_idx;
+  int64_t col_cap;
+  int32_t* nnz;
+  int32_t* tile_order;
+  int32_t npairs, qb_per_unit, group_heads;
+  uint32_t* err;
+};
+
+// Launch the attention kernel for one head dimension (defined in
+// attn_d{64,96,128}.cu). maps = {Q, K, V} tensor maps.
+cudaError_t launch_attn_d64(int block, bool sparse, const CUtensorMap* maps, const AttnParams& p, cudaStream_t st);
+cudaError_t launch_attn_d96(int block, bool sparse, const CUtensorMap* maps, const AttnParams& p, cudaStream_t st);
+cudaError_t launch_attn_d128(int block, bool sparse, const CUtensorMap* maps, const AttnParams& p, cudaStream_t st);
+
+cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream);
+
+}  // namespace wise

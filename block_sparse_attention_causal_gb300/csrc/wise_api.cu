@@ -1,0 +1,325 @@
+// C ABI of libwise (declared in include/wise.h): argument validation, TMA
+// descriptor encoding, workspace sizing, dispatch to the kernels, and the
+// device error word.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "wise.h"
+
+// The one piece of library state: a per-device word that kernels OR error
+// bits into (bounded-wait timeouts, malformed supports).
+__device__ uint32_t g_wise_error_word;
+
+namespace wise {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxBlocks = 1024;
+constexpr size_t kL2GroupBytes = 32ull << 20;  // K/V bytes kept hot per group of heads
+
+std::mutex g_mu;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+// Device address of g_wise_error_word on the current device (looked up once).
+uint32_t* error_word() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_wise_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+// 2D view [rows = batch*heads*seq_len, head_dim] of a bf16 tensor; boxes of
+// `box_rows` rows and 64 (128B swizzle) or 32 (64B swizzle, head_dim 96)
+// columns.
+int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int d, int box_rows) {
+  auto enc = encoder();
+  if (!enc) return WISE_ERR_CUDA;
+  const int ch = (d == 96) ? 32 : 64;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {(cuuint32_t)ch, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, ch == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? WISE_OK : WISE_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_desc(const wise_attn_desc* d) {
+  if (!d) return WISE_ERR_INVALID_ARGUMENT;
+  if (d->batch < 1 || d->heads < 1 || d->seq_len < 1 || d->block < 1) return WISE_ERR_INVALID_ARGUMENT;
+  if (d->out_dtype != WISE_BF16 && d->out_dtype != WISE_F32) return WISE_ERR_INVALID_ARGUMENT;
+  if (!(d->softmax_scale >= 0.f) || isinf(d->softmax_scale)) return WISE_ERR_INVALID_ARGUMENT;
+  if (d->seq_len % d->block != 0) return WISE_ERR_INVALID_ARGUMENT;
+  if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128) return WISE_ERR_UNSUPPORTED;
+  if (d->block != 64 && d->block != 128) return WISE_ERR_UNSUPPORTED;
+  if (d->seq_len / d->block > kMaxBlocks) return WISE_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)d->batch * d->heads * d->seq_len;
+  if (rows + 256 > INT32_MAX) return WISE_ERR_UNSUPPORTED;
+  return WISE_OK;
+}
+
+struct Shape {
+  int64_t bh;
+  int n, d, bn, nb, n_qtiles, npairs, group_heads;
+  int64_t n_units;
+};
+
+Shape shape_of(const wise_attn_desc* d) {
+  Shape s;
+  s.bh = (int64_t)d->batch * d->heads;
+  s.n = d->seq_len;
+  s.d = d->head_dim;
+  s.bn = d->block;
+  s.nb = d->seq_len / d->block;
+  s.n_qtiles = (d->seq_len + 127) / 128;
+  s.npairs = (s.n_qtiles + 1) / 2;
+  const size_t kv_per_head = (size_t)2 * d->seq_len * d->head_dim * 2;
+  int64_t g = (int64_t)(kL2GroupBytes / kv_per_head);
+  if (g < 1) g = 1;
+  if (g > s.bh) g = s.bh;
+  s.group_heads = (int)g;
+  s.n_units = s.bh * s.npairs;
+  return s;
+}
+
+size_t lam_bytes(const Shape& s) {
+  const int64_t ept = 128 / s.bn;
+  const int64_t per_bh = ept * (int64_t)s.n_qtiles * (s.n_qtiles + 1) / 2;
+  return (size_t)(s.bh * per_bh * 128 * sizeof(float));
+}
+
+int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,
+                     float* mass, void* ws, const int32_t* row_ptr, const int32_t* col_idx, int64_t col_cap,
+                     const int32_t* tile_order, bool sparse, cudaStream_t stream) {
+  const Shape s = shape_of(desc);
+  uint32_t* err = error_word();
+  if (!err) return WISE_ERR_CUDA;
+  CUtensorMap maps[3];
+  const int64_t rows = s.bh * s.n;
+  int st = encode_map(&maps[0], q, rows, s.d, 128);
+  if (st == WISE_OK) st = encode_map(&maps[1], k, rows, s.d, s.bn);
+  if (st == WISE_OK) st = encode_map(&maps[2], v, rows, s.d, s.bn);
+  if (st != WISE_OK) return st;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.bh_count = (int32_t)s.bh;
+  p.n = s.n;
+  p.nb = s.nb;
+  p.n_qtiles = s.n_qtiles;
+  p.npairs = s.npairs;
+  p.group_heads = s.group_heads;
+  const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / sqrtf((float)s.d);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out_f32 = desc->out_dtype == WISE_F32;
+  p.o = o;
+  p.lse = lse;
+  p.mass = mass;
+  p.lam = static_cast<float*>(ws);
+  p.row_ptr = row_ptr;
+  p.col_idx = col_idx;
+  p.col_cap = col_cap;
+  p.tile_order = tile_order;
+  p.n_units = s.n_units;
+  p.err = err;
+  cudaError_t e;
+  switch (s.d) {
+    case 64: e = launch_attn_d64(s.bn, sparse, maps, p, stream); break;
+    case 96: e = launch_attn_d96(s.bn, sparse, maps, p, stream); break;
+    default: e = launch_attn_d128(s.bn, sparse, maps, p, stream); break;
+  }
+  return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
+}
+
+int64_t fixed_point(double x) { return llrint(x * 4503599627370496.0); }  // x * 2^52, nearest even
+
+}  // namespace
+}  // namespace wise
+
+using namespace wise;
+
+extern "C" {
+
+int wise_abi_version(void) { return WISE_ABI_VERSION; }
+
+const char* wise_status_str(int status) {
+  switch (status) {
+    case WISE_OK: return "ok";
+    case WISE_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case WISE_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+    case WISE_ERR_ALIGNMENT: return "tensor base address not 16-byte aligned";
+    case WISE_ERR_WORKSPACE: return "workspace missing or too small";
+    case WISE_ERR_BAD_SUPPORT: return "malformed support (CSR) or schedule";
+    case WISE_ERR_CUDA: return "CUDA error";
+    case WISE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t wise_attn_discover_workspace(const wise_attn_desc* desc) {
+  if (check_desc(desc) != WISE_OK) return 0;
+  return lam_bytes(shape_of(desc));
+}
+
+int64_t wise_schedule_units(const wise_attn_desc* desc) {
+  if (check_desc(desc) != WISE_OK) return 0;
+  return shape_of(desc).n_units;
+}
+
+int64_t wise_support_capacity(const wise_attn_desc* desc) {
+  if (check_desc(desc) != WISE_OK) return 0;
+  const Shape s = shape_of(desc);
+  return s.bh * (int64_t)s.nb * (s.nb + 1) / 2;
+}
+
+size_t wise_select_workspace(const wise_attn_desc* desc, int32_t window) {
+  if (check_desc(desc) != WISE_OK || window < 1 || window > 8) return 0;
+  const Shape s = shape_of(desc);
+  const int64_t rows = s.bh * s.nb;
+  const int64_t words = (s.nb + 31) / 32;
+  return (size_t)(rows * words * 4 + rows * 4 + 256);
+}
+
+int wise_attn_discover(const wise_attn_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,
+                       float* block_mass, void* workspace, size_t workspace_bytes, wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!q || !k || !v || !o) return WISE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return WISE_ERR_ALIGNMENT;
+  if ((lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (block_mass && (reinterpret_cast<uintptr_t>(block_mass) & 3u)))
+    return WISE_ERR_ALIGNMENT;
+  if (block_mass) {
+    const size_t need = lam_bytes(shape_of(desc));
+    if (!workspace || workspace_bytes < need) return WISE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return WISE_ERR_ALIGNMENT;
+  }
+  return launch_attention(desc, q, k, v, o, lse, block_mass, workspace, nullptr, nullptr, 0, nullptr, false,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wise_attn_sparse(const wise_attn_desc* desc, const void* q, const void* k, const void* v, const int32_t* row_ptr,
+                     const int32_t* col_idx, int64_t col_capacity, const int32_t* tile_order, void* o, float* lse,
+                     wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!q || !k || !v || !o || !row_ptr || !col_idx || col_capacity < 0) return WISE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return WISE_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(row_ptr) & 3u) || (reinterpret_cast<uintptr_t>(col_idx) & 3u) ||
+      (tile_order && (reinterpret_cast<uintptr_t>(tile_order) & 3u)) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return WISE_ERR_ALIGNMENT;
+  return launch_attention(desc, q, k, v, o, lse, nullptr, nullptr, row_ptr, col_idx, col_capacity, tile_order, true,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int32_t window, double eta,
+                        uint32_t flags, int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity, int32_t* tile_order,
+                        int32_t* nnz, void* workspace, size_t workspace_bytes, wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!block_mass || !row_ptr || !col_idx) return WISE_ERR_INVALID_ARGUMENT;
+  if (window < 1 || window > 8 || !(eta > 0.0 && eta < 1.0) || (flags & ~3u)) return WISE_ERR_INVALID_ARGUMENT;
+  if (col_capacity < wise_support_capacity(desc)) return WISE_ERR_BAD_SUPPORT;
+  const size_t need = wise_select_workspace(desc, window);
+  if (!workspace || workspace_bytes < need) return WISE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) || (reinterpret_cast<uintptr_t>(block_mass) & 3u) ||
+      (reinterpret_cast<uintptr_t>(row_ptr) & 3u) || (reinterpret_cast<uintptr_t>(col_idx) & 3u))
+    return WISE_ERR_ALIGNMENT;
+  uint32_t* err = error_word();
+  if (!err) return WISE_ERR_CUDA;
+  const Shape s = shape_of(desc);
+  const int64_t rows = s.bh * s.nb;
+  const int64_t words = (s.nb + 31) / 32;
+  SelectLaunch sl;
+  sl.mass = block_mass;
+  sl.window = window;
+  sl.bh_count = (int32_t)s.bh;
+  sl.nb = s.nb;
+  sl.target_fx = fixed_point(eta);
+  sl.tol_fx = fixed_point(1e-6);
+  sl.flags = flags;
+  sl.bits = static_cast<uint32_t*>(workspace);
+  sl.counts = reinterpret_cast<int32_t*>(static_cast<uint32_t*>(workspace) + rows * words);
+  sl.row_ptr = row_ptr;
+  sl.col_idx = col_idx;
+  sl.col_cap = col_capacity;
+  sl.nnz = nnz;
+  sl.tile_order = tile_order;
+  sl.npairs = s.npairs;
+  sl.qb_per_unit = 256 / s.bn;
+  sl.group_heads = s.group_heads;
+  sl.err = err;
+  cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
+}
+
+int wise_validate_support(const wise_attn_desc* desc, const int32_t* row_ptr, const int32_t* col_idx,
+                          uint32_t flags) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!row_ptr || (!col_idx && row_ptr[0] != 0)) return WISE_ERR_INVALID_ARGUMENT;
+  const Shape s = shape_of(desc);
+  const int64_t rows = s.bh * s.nb;
+  if (row_ptr[0] != 0) return WISE_ERR_BAD_SUPPORT;
+  for (int64_t r = 0; r < rows; ++r) {
+    const int32_t a = row_ptr[r], b = row_ptr[r + 1];
+    if (b < a) return WISE_ERR_BAD_SUPPORT;
+    const int q = (int)(r % s.nb);
+    int prev = -1;
+    bool has0 = false, hasq = false;
+    for (int32_t j = a; j < b; ++j) {
+      const int32_t c = col_idx[j];
+      if (c <= prev || c > q) return WISE_ERR_BAD_SUPPORT;
+      has0 |= (c == 0);
+      hasq |= (c == q);
+      prev = c;
+    }
+    if (((flags & WISE_SUPPORT_SINK) && !has0) || ((flags & WISE_SUPPORT_DIAG) && !hasq)) return WISE_ERR_BAD_SUPPORT;
+  }
+  return WISE_OK;
+}
+
+int wise_device_status(wise_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return WISE_ERR_CUDA;
+  uint32_t word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_wise_error_word, sizeof(word)) != cudaSuccess) return WISE_ERR_CUDA;
+  if (word && cudaMemcpyToSymbol(g_wise_error_word, &zero, sizeof(zero)) != cudaSuccess) return WISE_ERR_CUDA;
+  if (word & kErrTimeout) return WISE_ERR_DEVICE_TIMEOUT;
+  if (word & kErrBadSupport) return WISE_ERR_BAD_SUPPORT;
+  return WISE_OK;
+}
+
+}  // extern "C"

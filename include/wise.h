@@ -1,0 +1,191 @@
+/*
+ * wise.h -- C ABI of the GB300 (sm_103a) WISE block-sparse causal attention
+ * library: discover early, select a block support once, reuse it late.
+ *
+ * The operations follow "Attention Routing Stabilizes Early: Working-Set
+ * Inference for Recurrent Language Models" (WISE, arXiv 2609.27373):
+ *
+ *   wise_attn_discover   §3 Eq 2 (unrestricted causal attention during the
+ *                        first t_d recurrent steps) plus §5.1 Eq 5 (block
+ *                        mass r_qb) fused into the same kernel;
+ *   wise_select_support  §5.1 Eq 6 (per-step cumulative-mass block support,
+ *                        unioned over the discovery window) and Appendix B
+ *                        "Sparse-kernel implementation" (support stored as a
+ *                        GPU-resident CSR of row offsets and block indices,
+ *                        built once after discovery);
+ *   wise_attn_sparse     §5.2 Eqs 7-8 (late-step attention restricted to the
+ *                        reused support; Q/K/V and the within-support softmax
+ *                        are recomputed on every call).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Tensors are dense, row-major, in device memory owned by the caller:
+ *     Q, K, V, O : [batch, heads, seq_len, head_dim], head_dim contiguous;
+ *     LSE        : [batch, heads, seq_len] float32, natural-log
+ *                  log-sum-exp of the scaled scores of each query row;
+ *     block mass : [batch, heads, nb, nb] float32, nb = seq_len / block,
+ *                  row q = query block, column b = key block (zero for b > q).
+ *   Q, K, V are bf16. O is bf16 or float32 (wise_attn_desc.out_dtype).
+ * - Masking is causal: key j is admissible for query i iff j <= i; key block
+ *   b is admissible for query block q iff b <= q. One call is one attention
+ *   layer with as many key/value heads as query heads.
+ * - Supported shapes: head_dim in {64, 96, 128}; block in {64, 128};
+ *   seq_len a positive multiple of block with seq_len / block <= 1024;
+ *   batch * heads >= 1. Base pointers of Q/K/V/O must be 16-byte aligned.
+ * - The library never allocates or frees memory and keeps no state besides
+ *   one device error word per GPU. Calls are asynchronous and ordered on the
+ *   given stream (a cudaStream_t; NULL means the legacy default stream).
+ * - Argument, shape and alignment errors are reported before any launch and
+ *   nothing is written. A failed launch returns WISE_ERR_CUDA. Kernel-side
+ *   problems (a malformed support list, a wait that timed out) are recorded in
+ *   the device error word and read back with wise_device_status().
+ */
+#ifndef WISE_H_
+#define WISE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WISE_ABI_VERSION 1
+
+typedef struct CUstream_st* wise_stream_t; /* same type as cudaStream_t */
+
+typedef enum wise_status {
+  WISE_OK = 0,
+  WISE_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad shape, bad eta, ...   */
+  WISE_ERR_UNSUPPORTED = 2,      /* valid but not built (head_dim, block)   */
+  WISE_ERR_ALIGNMENT = 3,        /* a tensor base is not 16-byte aligned     */
+  WISE_ERR_WORKSPACE = 4,        /* workspace missing or too small           */
+  WISE_ERR_BAD_SUPPORT = 5,      /* support CSR malformed / over capacity    */
+  WISE_ERR_CUDA = 6,             /* CUDA runtime or driver error             */
+  WISE_ERR_DEVICE_TIMEOUT = 7    /* a kernel wait exceeded its time limit    */
+} wise_status;
+
+typedef enum wise_dtype { WISE_BF16 = 0, WISE_F32 = 1 } wise_dtype;
+
+/* Support flags (readings of this library, not part of Eq 6 itself). */
+#define WISE_SUPPORT_SINK 1u /* add key block 0, which holds the first token  */
+#define WISE_SUPPORT_DIAG 2u /* add the diagonal key block b = q              */
+
+typedef struct wise_attn_desc {
+  int32_t batch;
+  int32_t heads;
+  int32_t seq_len;       /* n */
+  int32_t head_dim;      /* d_h */
+  int32_t block;         /* B, the support block size (query and key blocks) */
+  float softmax_scale;   /* 0 => 1/sqrt(head_dim), the scale of Eq 2 */
+  int32_t out_dtype;     /* wise_dtype of O */
+} wise_attn_desc;
+
+/* ABI version (WISE_ABI_VERSION) and a static string for a status code. */
+int wise_abi_version(void);
+const char* wise_status_str(int status);
+
+/* Bytes of workspace wise_attn_discover needs when block_mass != NULL
+ * (per-row, per-key-block partial log-sum-exp values); 0 when the
+ * descriptor is invalid. */
+size_t wise_attn_discover_workspace(const wise_attn_desc* desc);
+
+/*
+ * wise_attn_discover -- one early (discovery) recurrent step.
+ * Computes O = softmax(Q K^T * scale + M) V with the causal mask M (§3 Eq 2)
+ * and, when block_mass != NULL, the block masses of §5.1 Eq 5:
+ *     r_qb = (1/B) * sum_{i in query block q} sum_{j in key block b} A_ij,
+ * written as [batch, heads, nb, nb] float32 (every entry is written; entries
+ * with b > q are zero, and each row sums to 1 up to rounding).
+ *   q, k, v     : bf16 inputs (device).
+ *   o           : output (device), dtype desc->out_dtype.
+ *   lse         : optional float32 [batch, heads, seq_len] (device) or NULL.
+ *   block_mass  : optional float32 masses (device) or NULL.
+ *   workspace   : device buffer of wise_attn_discover_workspace(desc) bytes
+ *                 when block_mass != NULL; ignored otherwise. Its contents
+ *                 are scratch and need no initialisation.
+ * Returns WISE_OK or an error status (nothing launched on error).
+ */
+int wise_attn_discover(const wise_attn_desc* desc, const void* q, const void* k, const void* v,
+                       void* o, float* lse, float* block_mass, void* workspace,
+                       size_t workspace_bytes, wise_stream_t stream);
+
+/* Number of work units of the late-step kernel: the length of the
+ * tile_order schedule (one unit = 256 consecutive query rows of one
+ * (batch, head)); 0 when the descriptor is invalid. */
+int64_t wise_schedule_units(const wise_attn_desc* desc);
+
+/* Maximum number of CSR entries a support can hold:
+ * batch * heads * nb * (nb + 1) / 2 (every admissible block). */
+int64_t wise_support_capacity(const wise_attn_desc* desc);
+
+/* Bytes of workspace wise_select_support needs for `window` mass tensors. */
+size_t wise_select_workspace(const wise_attn_desc* desc, int32_t window);
+
+/*
+ * wise_select_support -- build the reused working set once after discovery.
+ * For every (batch, head, query block q) and each of the `window` mass
+ * tensors (the last min(4, t_d) discovery steps, §5.1 Eq 6 / Appendix B
+ * Eq 18), takes the smallest set of admissible key blocks (b <= q) whose
+ * cumulative mass reaches eta, blocks ordered by descending mass; the
+ * support is the union over the window, plus key block 0 if
+ * WISE_SUPPORT_SINK and block q if WISE_SUPPORT_DIAG is set in `flags`.
+ * Cumulative sums run in int64 fixed point (2^-52 units, masses rounded to
+ * nearest even); near-ties within 1e-6 of the k-th mass go to the lower
+ * block index; if the admissible mass never reaches eta every admissible
+ * block is taken.
+ *   block_mass : float32 [window, batch, heads, nb, nb] (device).
+ *   window     : 1..8.   eta: 0 < eta < 1.
+ *   row_ptr    : int32 [batch*heads*nb + 1] (device), rows ordered
+ *                (batch, head, query block); row_ptr[0] = 0.
+ *   col_idx    : int32 [col_capacity] (device), ascending key blocks per
+ *                row. col_capacity must be >= wise_support_capacity(desc).
+ *   tile_order : int32 [wise_schedule_units(desc)] (device) or NULL: the
+ *                late-step work order (execution metadata for
+ *                wise_attn_sparse: heads in L2-sized groups, heavier units
+ *                first within a group).
+ *   nnz        : int32 [1] (device) or NULL: total number of entries.
+ *   workspace  : wise_select_workspace(desc, window) bytes (device).
+ */
+int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int32_t window,
+                        double eta, uint32_t flags, int32_t* row_ptr, int32_t* col_idx,
+                        int64_t col_capacity, int32_t* tile_order, int32_t* nnz,
+                        void* workspace, size_t workspace_bytes, wise_stream_t stream);
+
+/*
+ * wise_attn_sparse -- one late (reuse) recurrent step, §5.2 Eq 8:
+ * O = softmax(Q K^T * scale + M + R) V where R is 0 on the key blocks listed
+ * for the query's block and -inf elsewhere (Eq 7); M is causal. Only the
+ * listed key blocks are read and computed.
+ *   row_ptr, col_idx : the support CSR (device), as written by
+ *                wise_select_support or by the caller (same layout; blocks
+ *                strictly ascending and <= q within each row).
+ *   col_capacity     : number of int32 entries readable at col_idx.
+ *   tile_order       : the schedule from wise_select_support, or NULL for
+ *                the natural order.
+ *   o, lse           : as in wise_attn_discover. A row whose support admits
+ *                no key gets O = 0 and LSE = -inf.
+ * Entries that break the CSR rules are skipped and flagged in the device
+ * error word (WISE_ERR_BAD_SUPPORT); they are never dereferenced out of
+ * bounds.
+ */
+int wise_attn_sparse(const wise_attn_desc* desc, const void* q, const void* k, const void* v,
+                     const int32_t* row_ptr, const int32_t* col_idx, int64_t col_capacity,
+                     const int32_t* tile_order, void* o, float* lse, wise_stream_t stream);
+
+/* Host-side check of a support CSR (host pointers): row_ptr monotone from 0,
+ * every row strictly ascending with 0 <= b <= q, and, if the flags ask for
+ * them, block 0 and block q present. Returns WISE_OK or
+ * WISE_ERR_BAD_SUPPORT. */
+int wise_validate_support(const wise_attn_desc* desc, const int32_t* row_ptr_host,
+                          const int32_t* col_idx_host, uint32_t flags);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device: WISE_OK, WISE_ERR_BAD_SUPPORT, WISE_ERR_DEVICE_TIMEOUT, or
+ * WISE_ERR_CUDA if the synchronisation itself failed. */
+int wise_device_status(wise_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WISE_H_ */

@@ -1,0 +1,119 @@
+"""The C-ABI library loads, exports every symbol the header declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from block_sparse_attention_causal_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "wise.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wise_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_exactly_the_binding_exports():
+    assert _declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.wise_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.wise_status_str(s).decode()
+    assert lib.wise_status_str(99).decode() == "unknown status"
+
+
+def _desc(b=1, h=2, n=256, d=64, blk=64, scale=0.0, out=0):
+    return _lib.make_desc(b, h, n, d, blk, scale, out)
+
+
+def test_workspace_and_capacity_queries(lib):
+    d = _desc(1, 2, 256, 64, 64)
+    nb = 4
+    assert lib.wise_support_capacity(d) == 2 * nb * (nb + 1) // 2
+    # two 128-row tiles per unit; n = 256 -> one unit per (batch, head)
+    assert lib.wise_schedule_units(d) == 2
+    # lambda scratch: (128/B) * T(T+1)/2 entries of 128 floats per (b,h), T = 2 query tiles
+    assert lib.wise_attn_discover_workspace(d) == 2 * (2 * 3) * 128 * 4
+    assert lib.wise_select_workspace(d, 2) > 0
+    assert lib.wise_select_workspace(d, 0) == 0
+    assert lib.wise_schedule_units(_desc(1, 1, 128 * 5, 128, 128)) == 3
+
+
+@pytest.mark.parametrize("bad", [
+    dict(b=0), dict(h=0), dict(n=0), dict(n=100), dict(blk=0), dict(scale=-1.0), dict(out=7),
+])
+def test_invalid_descriptor_rejected(lib, bad):
+    d = _desc(**bad)
+    assert lib.wise_support_capacity(d) == 0
+    st = lib.wise_attn_discover(d, 16, 16, 16, 16, None, None, None, 0, None)
+    assert st == _lib.WISE_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("bad", [dict(d=80), dict(d=256), dict(blk=32), dict(blk=256), dict(n=64 * 2048)])
+def test_unsupported_shapes_rejected(lib, bad):
+    d = _desc(**bad)
+    assert lib.wise_attn_discover(d, 16, 16, 16, 16, None, None, None, 0, None) == _lib.WISE_ERR_UNSUPPORTED
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    d = _desc()
+    assert lib.wise_attn_discover(d, None, 16, 16, 16, None, None, None, 0, None) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert lib.wise_attn_discover(d, 8, 16, 16, 16, None, None, None, 0, None) == _lib.WISE_ERR_ALIGNMENT
+    # block masses requested without workspace
+    assert lib.wise_attn_discover(d, 16, 16, 16, 16, None, 16, None, 0, None) == _lib.WISE_ERR_WORKSPACE
+    assert lib.wise_attn_sparse(d, 16, 16, 16, None, 16, 10, None, 16, None, None) == _lib.WISE_ERR_INVALID_ARGUMENT
+
+
+def test_select_argument_checks(lib):
+    d = _desc()
+    cap = lib.wise_support_capacity(d)
+    ws = lib.wise_select_workspace(d, 2)
+    args = lambda **kw: dict(dict(mass=16, window=2, eta=0.9, flags=3, cap=cap, ws=16, wsb=ws), **kw)
+
+    def call(a):
+        return lib.wise_select_support(d, a["mass"], a["window"], a["eta"], a["flags"], 16, 16, a["cap"], None,
+                                       None, a["ws"], a["wsb"], None)
+    assert call(args(eta=0.0)) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert call(args(eta=1.0)) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert call(args(window=0)) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert call(args(window=9)) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert call(args(flags=4)) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert call(args(mass=None)) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert call(args(cap=cap - 1)) == _lib.WISE_ERR_BAD_SUPPORT
+    assert call(args(wsb=ws - 1)) == _lib.WISE_ERR_WORKSPACE
+
+
+def _host(a):
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a, a.ctypes.data
+
+
+def test_host_support_validator(lib):
+    d = _desc(1, 1, 256, 64, 64)  # nb = 4
+    good_rows = [[0], [0, 1], [0, 2], [0, 1, 3]]
+    rp = np.cumsum([0] + [len(r) for r in good_rows]).astype(np.int32)
+    ci = np.array(sum(good_rows, []), np.int32)
+    assert lib.wise_validate_support(d, rp.ctypes.data, ci.ctypes.data, 3) == _lib.WISE_OK
+    for bad_rows in ([[0], [1, 0], [0, 2], [0, 3]],      # not ascending
+                     [[0], [0, 1], [0, 3], [0, 1, 3]],   # block above the diagonal
+                     [[0], [0, 1], [0, 2], [0, 1]]):     # missing diagonal with DIAG
+        rp2 = np.cumsum([0] + [len(r) for r in bad_rows]).astype(np.int32)
+        ci2 = np.array(sum(bad_rows, []), np.int32)
+        assert lib.wise_validate_support(d, rp2.ctypes.data, ci2.ctypes.data, 3) == _lib.WISE_ERR_BAD_SUPPORT
+    rows_nodiag = [[0], [0], [0], [0, 1]]
+    rp3 = np.cumsum([0] + [len(r) for r in rows_nodiag]).astype(np.int32)
+    ci3 = np.array(sum(rows_nodiag, []), np.int32)
+    assert lib.wise_validate_support(d, rp3.ctypes.data, ci3.ctypes.data, 1) == _lib.WISE_OK
+    assert lib.wise_validate_support(d, rp3.ctypes.data, ci3.ctypes.data, 3) == _lib.WISE_ERR_BAD_SUPPORT

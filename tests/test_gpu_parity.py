@@ -1,0 +1,318 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Gates: O max-abs <= 1e-2 (float32 output; bf16 output adds half a bf16 ulp
+of the reference), LSE <= 1e-3, block masses <= 1e-3, support CSR bit-exact
+when both sides select from the same masses. Inputs are seeded and rounded
+to bf16 before either side sees them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_causal_gb300 as wise
+import workloads as wl
+from oracle import wise_oracle as O
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
+
+O_TOL, LSE_TOL, MASS_TOL = 1e-2, 1e-3, 1e-3
+
+
+def _bf16_inputs(b, h, n, d, seed, scale=1.0, planted=0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((3, b, h, n, d)).astype(np.float32) * np.float32(scale)
+    if planted:
+        # a shared direction in Q and in the keys of a few blocks, so masses are far from uniform
+        for bi in range(b):
+            for hi in range(h):
+                u = rng.standard_normal(d).astype(np.float32) * 2.0
+                x[0, bi, hi] += u
+                for blk in rng.choice(max(1, n // 64), size=min(planted, max(1, n // 64)), replace=False):
+                    x[1, bi, hi, blk * 64:(blk + 1) * 64] += u
+    x = wl.bf16_round(x)
+    t = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    return x, t[0].contiguous(), t[1].contiguous(), t[2].contiguous()
+
+
+def _oracle_discover(x, block):
+    return O.discover(x[0].astype(np.float64), x[1].astype(np.float64), x[2].astype(np.float64), block)
+
+
+def _assert_close(name, got, ref, tol):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin), f"{name}: non-finite pattern differs"
+    err = np.max(np.abs(got[fin] - ref[fin])) if fin.any() else 0.0
+    assert err <= tol, f"{name}: max abs error {err:.3e} > {tol:.1e}"
+    return err
+
+
+SHAPES = [  # (batch, heads, n, d, block)
+    (1, 2, 256, 64, 64),
+    (1, 1, 64, 64, 64),      # a single block; one partial 128-row tile
+    (2, 1, 192, 96, 64),     # odd number of 64-blocks: ragged last tile
+    (1, 2, 384, 128, 128),   # odd number of 128-row tiles
+    (1, 1, 640, 128, 128),
+    (1, 1, 512, 96, 128),
+    (1, 3, 128, 64, 128),    # nb = 1
+    (2, 2, 320, 128, 64),
+    (1, 1, 1024, 64, 128),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_discover_parity(shape):
+    b, h, n, d, blk = shape
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=n + d + blk, scale=1.5, planted=2)
+    o, lse, mass = wise.discover(q, k, v, blk, out_dtype=torch.float32)
+    wise.check_device()
+    o_ref, lse_ref, r_ref = _oracle_discover(x, blk)
+    _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
+    _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+    _assert_close("mass", mass.cpu().numpy(), r_ref, MASS_TOL)
+    iu = np.triu_indices(n // blk, 1)
+    assert np.all(mass.cpu().numpy()[..., iu[0], iu[1]] == 0.0)
+
+
+def test_discover_bf16_output_within_half_ulp():
+    x, q, k, v = _bf16_inputs(1, 2, 512, 128, 128, seed=5, scale=2.0, planted=3)
+    o, _, _ = wise.discover(q, k, v, 128, want_mass=False)
+    o_ref, _, _ = _oracle_discover(x, 128)
+    got = o.float().cpu().numpy()
+    # half a bf16 ulp of the reference value
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(o_ref), 1e-30))) - 8)
+    assert np.all(np.abs(got - o_ref) <= O_TOL + half_ulp)
+
+
+def test_discover_lse_optional_and_no_mass():
+    x, q, k, v = _bf16_inputs(1, 1, 256, 64, 64, seed=7)
+    o1, lse1, _ = wise.discover(q, k, v, 64, want_mass=False, want_lse=False, out_dtype=torch.float32)
+    o2, lse2, m2 = wise.discover(q, k, v, 64, out_dtype=torch.float32)
+    assert lse1 is None and torch.equal(o1, o2)
+
+
+def test_workload_tiny_discover():
+    cfg = wl.CONFIGS["tiny"]
+    x = wl.step_inputs(cfg, 0)
+    q, k, v = (torch.from_numpy(x[i]).to(torch.bfloat16).cuda() for i in range(3))
+    o, lse, mass = wise.discover(q, k, v, cfg.block, out_dtype=torch.float32)
+    o_ref, lse_ref, r_ref = _oracle_discover(x, cfg.block)
+    _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
+    _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+    _assert_close("mass", mass.cpu().numpy(), r_ref, MASS_TOL)
+
+
+# ------------------------------------------------------------ select (Eq 6)
+
+def _random_masses(w, b, h, nb, seed, ties=False):
+    rng = np.random.default_rng(seed)
+    m = np.zeros((w, b, h, nb, nb), np.float32)
+    for idx in np.ndindex(w, b, h):
+        for q in range(nb):
+            r = rng.dirichlet(np.full(q + 1, 0.3)).astype(np.float32)
+            if ties and q >= 3:
+                kind = rng.integers(0, 3)
+                if kind == 0:      # exact ties among a few blocks
+                    pick = rng.choice(q + 1, size=min(3, q + 1), replace=False)
+                    r[pick] = r[pick].mean()
+                elif kind == 1:    # near ties within the 1e-6 tolerance
+                    pick = rng.choice(q + 1, size=2, replace=False)
+                    r[pick[1]] = r[pick[0]] + np.float32(4e-7)
+            m[idx][q, :q + 1] = r
+    return m
+
+
+@pytest.mark.parametrize("case", [(2, 1, 2, 4, 64, 0.9), (3, 2, 3, 32, 128, 0.9), (4, 1, 2, 64, 128, 0.95),
+                                  (1, 1, 1, 1, 128, 0.5), (2, 1, 1, 300, 64, 0.8), (4, 1, 1, 1024, 64, 0.95)],
+                         ids=lambda c: "W%d_B%d_H%d_nb%d_blk%d_eta%s" % c)
+@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("flags", [0, 3])
+def test_select_bit_exact_on_same_masses(case, ties, flags):
+    w, b, h, nb, blk, eta = case
+    m = _random_masses(w, b, h, nb, seed=nb * 7 + w, ties=ties)
+    sup = wise.select_support(torch.from_numpy(m).cuda(), nb * blk, 64, blk, eta, flags)
+    wise.check_device()
+    rp_ref, ci_ref = O.select(m.astype(np.float64), eta, flags)
+    rp = sup.row_ptr.cpu().numpy()
+    assert np.array_equal(rp, rp_ref)
+    assert np.array_equal(sup.col_idx.cpu().numpy()[:rp[-1]], ci_ref)
+    assert int(sup.nnz.item()) == len(ci_ref)
+    _check_tile_order(sup)
+
+
+def _check_tile_order(sup):
+    lib = wise._lib.load()
+    desc = wise._lib.make_desc(sup.batch, sup.heads, sup.seq_len, sup.head_dim, sup.block)
+    units = int(lib.wise_schedule_units(desc))
+    order = sup.tile_order.cpu().numpy()[:units]
+    assert sorted(order.tolist()) == list(range(units))
+
+
+def test_select_on_gpu_masses_matches_oracle_select():
+    cfg = wl.CONFIGS["tiny"]
+    masses = []
+    for t in cfg.window_steps:
+        x = wl.step_inputs(cfg, t)
+        q, k, v = (torch.from_numpy(x[i]).to(torch.bfloat16).cuda() for i in range(3))
+        masses.append(wise.discover(q, k, v, cfg.block)[2])
+    m = torch.stack(masses).contiguous()
+    sup = wise.select_support(m, cfg.seq_len, cfg.head_dim, cfg.block, cfg.eta)
+    rp_ref, ci_ref = O.select(m.cpu().numpy().astype(np.float64), cfg.eta)
+    assert np.array_equal(sup.row_ptr.cpu().numpy(), rp_ref)
+    assert np.array_equal(sup.col_idx.cpu().numpy()[:len(ci_ref)], ci_ref)
+
+
+# ------------------------------------------------------------ sparse (Eq 8)
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("density", [0.15, 0.5])
+def test_sparse_parity_random_support(shape, density):
+    b, h, n, d, blk = shape
+    nb = n // blk
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=3 * n + d, scale=1.5, planted=2)
+    rng = np.random.default_rng(n + blk)
+    rows = []
+    for _ in range(b * h):
+        rows.extend(wl.random_support(nb, density, rng, sink=bool(rng.integers(0, 2)), diag=bool(rng.integers(0, 2))))
+    sup = wise.support_from_lists(rows, b, h, n, d, blk)
+    o, lse = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    wise.check_device()
+    rp, ci = O.support_to_csr(rows)
+    o_ref, lse_ref = O.sparse(x[0].astype(np.float64), x[1].astype(np.float64), x[2].astype(np.float64), blk, rp, ci)
+    _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
+    _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+
+
+def test_sparse_full_support_bitwise_equals_discover():
+    b, h, n, d, blk = 1, 2, 768, 128, 128
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=11, scale=1.5, planted=2)
+    nb = n // blk
+    rows = [list(range(qb + 1)) for _ in range(b * h) for qb in range(nb)]
+    sup = wise.support_from_lists(rows, b, h, n, d, blk)
+    o1, l1 = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    o2, l2, _ = wise.discover(q, k, v, blk, want_mass=False, out_dtype=torch.float32)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_sparse_empty_rows_give_zero_and_neg_inf():
+    b, h, n, d, blk = 1, 1, 512, 64, 128
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=2)
+    rows = [[0], [], [0, 2], []]
+    sup = wise.support_from_lists(rows, b, h, n, d, blk)
+    o, lse = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    wise.check_device()
+    on, ln = o.cpu().numpy(), lse.cpu().numpy()
+    assert np.all(on[0, 0, 128:256] == 0) and np.all(np.isneginf(ln[0, 0, 128:256]))
+    assert np.all(on[0, 0, 384:] == 0) and np.all(np.isneginf(ln[0, 0, 384:]))
+    rp, ci = O.support_to_csr(rows)
+    o_ref, _ = O.sparse(x[0].astype(np.float64), x[1].astype(np.float64), x[2].astype(np.float64), blk, rp, ci)
+    _assert_close("O", on, o_ref, O_TOL)
+
+
+def test_sparse_malformed_support_is_flagged_not_faulted():
+    b, h, n, d, blk = 1, 1, 512, 64, 128
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=4)
+    rows = [[0], [1, 0], [0, 7, 2], [-3, 3]]  # descending, above the diagonal, negative
+    sup = wise.support_from_lists(rows, b, h, n, d, blk)
+    wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    assert wise.device_status() == wise._lib.WISE_ERR_BAD_SUPPORT
+    assert wise.device_status() == wise._lib.WISE_OK  # the word is cleared by the read
+
+
+# ------------------------------------------------------------ trajectories
+
+def _run_trajectory(cfg, heads=None):
+    """GPU trajectory: t_d discovery steps (masses on the window), one
+    selection, late steps. Returns (support, per-step GPU outputs)."""
+    masses, outs = [], {}
+    for t in range(cfg.t_d):
+        x = wl.step_inputs(cfg, t, heads=heads)
+        q, k, v = (torch.from_numpy(x[i]).to(torch.bfloat16).cuda() for i in range(3))
+        o, lse, m = wise.discover(q, k, v, cfg.block, want_mass=t in cfg.window_steps, out_dtype=torch.float32)
+        if m is not None:
+            masses.append(m)
+        outs[t] = (x, o.cpu().numpy(), lse.cpu().numpy(), None if m is None else m.cpu().numpy())
+    sup = wise.select_support(torch.stack(masses).contiguous(), cfg.seq_len, cfg.head_dim, cfg.block, cfg.eta)
+    wise.check_device()
+    return sup, outs
+
+
+def _assert_support_matches(sup_rows, oracle_masses, cfg, head_rows):
+    """CSR rows from GPU masses vs the oracle's selection from oracle masses;
+    a difference is allowed only where Eq 13's margin is below 1e-4."""
+    ref_rows = O.working_set(oracle_masses, cfg.eta)
+    flips = 0
+    for qb, (got, ref) in enumerate(zip(head_rows, ref_rows)):
+        if got != ref:
+            margin = min(O.identification_margin(m[qb], qb, cfg.eta) for m in oracle_masses)
+            assert margin < 1e-4, f"support of query block {qb} differs with margin {margin:.2e}: {got} vs {ref}"
+            flips += 1
+    return flips
+
+
+def test_tiny_trajectory_end_to_end():
+    cfg = wl.CONFIGS["tiny"]
+    sup, outs = _run_trajectory(cfg)
+    rows = sup.to_lists()
+    nb = cfg.n_blocks
+    for bi in range(cfg.batch):
+        for hi in range(cfg.heads):
+            om = []
+            for t in cfg.window_steps:
+                x = outs[t][0]
+                _, _, r = O.causal_attention(*(x[i, bi, hi].astype(np.float64) for i in range(3)), cfg.block,
+                                             want_mass=True)
+                om.append(r)
+                _assert_close("mass", outs[t][3][bi, hi], r, MASS_TOL)
+            base = (bi * cfg.heads + hi) * nb
+            _assert_support_matches(rows[base:base + nb], om, cfg, rows[base:base + nb])
+    # late steps over the selected support
+    rp = sup.row_ptr.cpu().numpy()
+    ci = sup.col_idx.cpu().numpy()
+    for t in range(cfg.t_d, cfg.steps):
+        x = wl.step_inputs(cfg, t)
+        q, k, v = (torch.from_numpy(x[i]).to(torch.bfloat16).cuda() for i in range(3))
+        o, lse = wise.sparse(q, k, v, sup, out_dtype=torch.float32)
+        o_ref, lse_ref = O.sparse(x[0].astype(np.float64), x[1].astype(np.float64), x[2].astype(np.float64),
+                                  cfg.block, rp, ci)
+        _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
+        _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["4k", "16k_h40_d96"])
+def test_full_size_config_sampled(name):
+    """Full-size configuration, in the launch configuration the benchmark
+    times; checked on sampled heads and query blocks."""
+    cfg = wl.CONFIGS[name]
+    sample = [(0, 0), (0, cfg.heads - 1)]
+    sup, outs = _run_trajectory(cfg)
+    rows = sup.to_lists()
+    nb = cfg.n_blocks
+    qbs = sorted({0, 1, nb // 2, nb - 1})
+    for bi, hi in sample:
+        om = []
+        for t in cfg.window_steps:
+            x = outs[t][0]
+            xs = [x[i, bi, hi].astype(np.float64) for i in range(3)]
+            o_ref, lse_ref, r = O.causal_attention(*xs, cfg.block, want_mass=True)
+            om.append(r)
+            _assert_close("mass", outs[t][3][bi, hi], r, MASS_TOL)
+            _assert_close("O", outs[t][1][bi, hi], o_ref, O_TOL)
+        base = (bi * cfg.heads + hi) * nb
+        _assert_support_matches(rows[base:base + nb], om, cfg, rows[base:base + nb])
+    t = cfg.steps - 1
+    x = wl.step_inputs(cfg, t)
+    q, k, v = (torch.from_numpy(x[i]).to(torch.bfloat16).cuda() for i in range(3))
+    o, lse = wise.sparse(q, k, v, sup, out_dtype=torch.float32)
+    o, lse = o.cpu().numpy(), lse.cpu().numpy()
+    for bi, hi in sample:
+        base = (bi * cfg.heads + hi) * nb
+        supp = rows[base:base + nb]
+        xs = [x[i, bi, hi].astype(np.float64) for i in range(3)]
+        o_ref, lse_ref, _ = O.causal_attention(*xs, cfg.block, support=supp, query_blocks=qbs)
+        for qb in qbs:
+            s = slice(qb * cfg.block, (qb + 1) * cfg.block)
+            _assert_close("O", o[bi, hi, s], o_ref[s], O_TOL)
+            _assert_close("LSE", lse[bi, hi, s], lse_ref[s], LSE_TOL)

@@ -394,7 +394,10 @@ __global__ void __launch_bounds__(320, 1)
 
       TileCursor cur;
       make_cursor(cur, i);
-      float m_ref = -INFINITY, l = 0.f;
+      // l: fp32 row sum (for LSE and the block masses); lt: sum of the
+      // bf16-rounded P that the tensor core multiplies (normalises O, so the
+      // output is an exact weighted mean of the rounded weights)
+      float m_ref = -INFINITY, l = 0.f, lt = 0.f;
       uint32_t cnt = 0;
       bool ok = true;
       int32_t blk;
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         // pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, written over S
-        float rs = 0.f;
+        float rs = 0.f, rt = 0.f;
 #pragma unroll
         for (int h = 0; h < BN / 64; ++h) {
           uint32_t s[2][32];
@@ -464,10 +467,12 @@ __global__ void __launch_bounds__(320, 1)
             }
             rs += p0 + p1;
             pk[j] = pack_bf16x2(p0, p1);
+            rt += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
           }
           tmem_st_x32(tS + h * 32, pk);
         }
         l = l * factor + rs;
+        lt = lt * factor + rt;
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -494,7 +499,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (ok) {
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const float inv_l = (lt > 0.f) ? 1.f / lt : 0.f;
         const size_t grow = (size_t)bh * p.n + qpos;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {

@@ -76,7 +76,7 @@ def test_discover_parity(shape):
 
 
 def test_discover_bf16_output_within_half_ulp():
-    x, q, k, v = _bf16_inputs(1, 2, 512, 128, 128, seed=5, scale=2.0, planted=3)
+    x, q, k, v = _bf16_inputs(1, 2, 512, 128, seed=5, scale=2.0, planted=3)
     o, _, _ = wise.discover(q, k, v, 128, want_mass=False)
     o_ref, _, _ = _oracle_discover(x, 128)
     got = o.float().cpu().numpy()
@@ -86,7 +86,7 @@ def test_discover_bf16_output_within_half_ulp():
 
 
 def test_discover_lse_optional_and_no_mass():
-    x, q, k, v = _bf16_inputs(1, 1, 256, 64, 64, seed=7)
+    x, q, k, v = _bf16_inputs(1, 1, 256, 64, seed=7)
     o1, lse1, _ = wise.discover(q, k, v, 64, want_mass=False, want_lse=False, out_dtype=torch.float32)
     o2, lse2, m2 = wise.discover(q, k, v, 64, out_dtype=torch.float32)
     assert lse1 is None and torch.equal(o1, o2)

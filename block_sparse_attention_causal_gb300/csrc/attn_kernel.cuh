@@ -412,8 +412,9 @@ __global__ void __launch_bounds__(320, 1)
         // columns c <= limit are admissible (causal mask M, working-set mask R)
         const int limit = row_on ? ((kbase + BN - 1 > qpos) ? qpos - kbase : BN) : -1;
         const bool full = limit >= BN - 1;
-        // pass 1: row max, 64 columns at a time (keeps register use low)
-        float mx = -INFINITY;
+        // pass 1: row max, 64 columns at a time (keeps register use low);
+        // four independent 3-input max chains
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int h = 0; h < BN / 64; ++h) {
           uint32_t s[2][32];
@@ -421,20 +422,19 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld_x32(tS + h * 64 + 32, s[1]);
           tmem_wait_ld(s[0]);
           tmem_wait_ld(s[1]);
-          if (full) {
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-              for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(s[cc][j]));
-          } else {
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                mx = fmaxf(mx, (h * 64 + cc * 32 + j <= limit) ? __uint_as_float(s[cc][j]) : -INFINITY);
+          for (int j = 0; j < 32; ++j) {
+            const int cc = j >> 4, jj = (j & 15) * 2;
+            float a = __uint_as_float(s[cc][jj]), b = __uint_as_float(s[cc][jj + 1]);
+            if (!full) {
+              const int c0 = h * 64 + 2 * j;
+              a = (c0 <= limit) ? a : -INFINITY;
+              b = (c0 + 1 <= limit) ? b : -INFINITY;
+            }
+            mx4[j & 3] = fmax3(mx4[j & 3], a, b);
           }
         }
-        mx *= sl2;
+        float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * sl2;
         float factor = 1.f;
         bool resc = false;
         if (cnt == 0) {
@@ -445,9 +445,12 @@ __global__ void __launch_bounds__(320, 1)
           resc = true;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, written over S
-        float rs = 0.f, rt = 0.f;
-#pragma unroll
+        // pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, written over S.
+        // Packed f32x2 FMA for the exponent argument and packed adds (two
+        // independent accumulators each) for the fp32 and bf16 row sums.
+        const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
+        uint64_t rs2[2] = {0ull, 0ull}, rt2[2] = {0ull, 0ull};
+#pragma unroll 1
         for (int h = 0; h < BN / 64; ++h) {
           uint32_t s[2][32];
           tmem_ld_x32(tS + h * 64, s[0]);
@@ -459,17 +462,27 @@ __global__ void __launch_bounds__(320, 1)
           for (int j = 0; j < 32; ++j) {
             const int cc = j >> 4, jj = (j & 15) * 2;
             const int c0 = h * 64 + 2 * j;
-            float p0 = fast_exp2(fmaf(__uint_as_float(s[cc][jj]), sl2, -m_use));
-            float p1 = fast_exp2(fmaf(__uint_as_float(s[cc][jj + 1]), sl2, -m_use));
+            float e0, e1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(s[cc][jj]), __uint_as_float(s[cc][jj + 1])), sc2, nm2), e0, e1);
+            float p0 = fast_exp2(e0);
+            float p1 = fast_exp2(e1);
             if (!full) {
               p0 = (c0 <= limit) ? p0 : 0.f;
               p1 = (c0 + 1 <= limit) ? p1 : 0.f;
             }
-            rs += p0 + p1;
             pk[j] = pack_bf16x2(p0, p1);
-            rt += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+            rs2[j & 1] = fadd2(rs2[j & 1], f2_pack(p0, p1));
+            rt2[j & 1] = fadd2(rt2[j & 1], f2_pack(__uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xFFFF0000u)));
           }
           tmem_st_x32(tS + h * 32, pk);
+        }
+        float rs, rt;
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(fadd2(rs2[0], rs2[1]), a0, a1);
+          f2_unpack(fadd2(rt2[0], rt2[1]), b0, b1);
+          rs = a0 + a1;
+          rt = b0 + b1;
         }
         l = l * factor + rs;
         lt = lt * factor + rt;

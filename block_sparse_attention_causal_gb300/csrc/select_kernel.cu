@@ -57,7 +57,8 @@ __device__ __forceinline__ int warp_sum32(int v) {
   return v;
 }
 
-// 8 warps per CTA, one row per warp.
+// 8 warps per CTA, one row per warp; NJ rounds of 32 blocks cover nb <= 32 NJ.
+template <int NJ>
 __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -69,32 +70,38 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
   uint32_t word = 0;  // word `lane` of the row's union bitmask
   for (int w = 0; w < p.window; ++w) {
     const float* src = p.mass + (((int64_t)w * p.bh_count + bh) * p.nb + q) * p.nb;
-    int64_t fx[32];
+    int64_t fx[NJ];
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
+    for (int jj = 0; jj < NJ; ++jj) {
       const int b = jj * 32 + lane;  // coalesced load order: jj-major
       fx[jj] = (b < nadm) ? __double2ll_rn((double)__ldg(src + b) * 4503599627370496.0) : INT64_MIN;
     }
-    int64_t total_pos = 0;
+    int64_t total_pos = 0, max_pos = 0;
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) total_pos += (fx[jj] > 0) ? fx[jj] : 0;
+    for (int jj = 0; jj < NJ; ++jj) {
+      total_pos += (fx[jj] > 0) ? fx[jj] : 0;
+      max_pos = max(max_pos, fx[jj]);
+    }
     total_pos = warp_sum64(total_pos);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) max_pos = max(max_pos, (int64_t)__shfl_xor_sync(0xffffffffu, max_pos, off));
     uint32_t sel_word_mine = 0;  // the word this lane will hold (word index = lane)
     if (total_pos < p.target_fx) {
       // Eq 6 cannot reach eta: every admissible block.
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
+      for (int jj = 0; jj < NJ; ++jj) {
         const uint32_t bal = __ballot_sync(0xffffffffu, fx[jj] != INT64_MIN);
         if (lane == jj) sel_word_mine = bal;
       }
     } else {
-      // largest v with sum_{fx >= v} fx >= target (v > 0 since target > 0)
+      // largest v with sum_{fx >= v} fx >= target (v > 0 since target > 0);
+      // v <= the largest mass, so bits above its top bit stay zero
       int64_t v = 0;
-      for (int bit = 62; bit >= 0; --bit) {
+      for (int bit = 63 - __clzll(max_pos); bit >= 0; --bit) {
         const int64_t cand = v | (int64_t(1) << bit);
         int64_t sacc = 0;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
+        for (int jj = 0; jj < NJ; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
         sacc = warp_sum64(sacc);
         if (sacc >= p.target_fx) v = cand;
       }
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
       int c_gt = 0, c_above = 0;
       const int64_t hi = v + p.tol_fx, lo = v - p.tol_fx;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
+      for (int jj = 0; jj < NJ; ++jj) {
         s_gt += (fx[jj] > v) ? fx[jj] : 0;
         c_gt += (fx[jj] > v) ? 1 : 0;
         c_above += (fx[jj] > hi) ? 1 : 0;
@@ -116,7 +123,7 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
       int slots = k - c_above;  // filled from the near-tie group, lowest index first
       int taken = 0;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
+      for (int jj = 0; jj < NJ; ++jj) {
         const bool above = fx[jj] != INT64_MIN && fx[jj] > hi;
         const bool near = fx[jj] != INT64_MIN && fx[jj] >= lo && fx[jj] <= hi;
         const uint32_t nb_bal = __ballot_sync(0xffffffffu, near);
@@ -259,7 +266,13 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   p.err = s.err;
   const int64_t rows = (int64_t)s.bh_count * s.nb;
   const unsigned grid_rows = (unsigned)((rows + 7) / 8);
-  select_rows_kernel<<<grid_rows, 256, 0, stream>>>(p);
+  const int rounds = (s.nb + 31) / 32;
+  if (rounds <= 1) select_rows_kernel<1><<<grid_rows, 256, 0, stream>>>(p);
+  else if (rounds <= 2) select_rows_kernel<2><<<grid_rows, 256, 0, stream>>>(p);
+  else if (rounds <= 4) select_rows_kernel<4><<<grid_rows, 256, 0, stream>>>(p);
+  else if (rounds <= 8) select_rows_kernel<8><<<grid_rows, 256, 0, stream>>>(p);
+  else if (rounds <= 16) select_rows_kernel<16><<<grid_rows, 256, 0, stream>>>(p);
+  else select_rows_kernel<32><<<grid_rows, 256, 0, stream>>>(p);
   scan_rows_kernel<<<1, 1024, 0, stream>>>(p);
   emit_rows_kernel<<<grid_rows, 256, 0, stream>>>(p);
   if (s.tile_order) {

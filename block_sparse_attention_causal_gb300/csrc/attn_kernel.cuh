@@ -8,11 +8,14 @@
 //    §5.2 Eqs 7-8 -- only listed key blocks are loaded and multiplied.
 //
 // One CTA = one work unit = two 128-row query tiles ("streams") of one
-// (batch, head). Warp roles (320 threads):
+// (batch, head). Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles once, then K/V blocks into an NST ring
 //   warp 1      TMEM allocator + MMA issuer (single thread)
-//   warps 2-5   softmax warpgroup of stream 0 (one query row per thread)
-//   warps 6-9   softmax warpgroup of stream 1
+//   warps 2-3   idle (the control warpgroup gives its registers away)
+//   warps 4-7   softmax warpgroup of stream 0 (one query row per thread)
+//   warps 8-11  softmax warpgroup of stream 1
+// Registers are moved from the control warpgroup (96 each) to the softmax
+// warpgroups (200 each): 128*96 + 256*200 <= 384*168, the launch allocation.
 // The MMA thread walks the ascending union of both streams' key-block lists;
 // a K/V block read by both streams is loaded once. Per stream, S = Q K^T goes
 // to its own TMEM columns; the softmax warps turn S into P (bf16, written
@@ -42,7 +45,11 @@ struct AttnCfg {
   static constexpr int NST_FIT = (int)((SMEM_BUDGET - 2u * Q_BYTES) / (2u * KV_BYTES));
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;  // K/V ring depth
   static_assert(NST >= 2, "ring");
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t REGS_CONTROL = 104, REGS_SOFTMAX = 200, REGS_LAUNCH = 168;
+  // setmaxnreg.inc waits for registers released by setmaxnreg.dec: the split
+  // must fit in what the CTA was launched with (checked against ptxas -v).
+  static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= THREADS * REGS_LAUNCH, "register split");
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2u * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
@@ -180,7 +187,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 }
 
 template <int D, int BN, bool SPARSE>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     wise_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   using C = AttnCfg<D, BN>;
@@ -253,7 +260,9 @@ __global__ void __launch_bounds__(320, 1)
     }
   };
 
-  if (warp == 0) {
+  if (warp < 4) {
+   setmaxnreg_dec<C::REGS_CONTROL>();
+   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -296,7 +305,7 @@ __global__ void __launch_bounds__(320, 1)
       if (has1) mbar_wait_drain(&q_full[1], 0, p.err);
     }
     __syncwarp();
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
@@ -375,9 +384,11 @@ __global__ void __launch_bounds__(320, 1)
       mbar_wait_drain(drain, 0, p.err);
     }
     __syncwarp();
+   }
   } else {
+    setmaxnreg_inc<C::REGS_SOFTMAX>();
     // ------------------------------------------------------------ softmax
-    const int i = (warp - 2) >> 2;
+    const int i = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
     if (!(i == 1 && !has1)) {
@@ -412,28 +423,26 @@ __global__ void __launch_bounds__(320, 1)
         // columns c <= limit are admissible (causal mask M, working-set mask R)
         const int limit = row_on ? ((kbase + BN - 1 > qpos) ? qpos - kbase : BN) : -1;
         const bool full = limit >= BN - 1;
-        // pass 1: row max, 64 columns at a time (keeps register use low);
-        // four independent 3-input max chains
+        // The whole S row (BN columns) is read from TMEM once; the row max and
+        // then P are computed from registers.
+        uint32_t s[BN / 32][32];
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld_x32(tS + cc * 32, s[cc]);
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) tmem_wait_ld(s[cc]);
+        if (!full) {
+#pragma unroll
+          for (int cc = 0; cc < BN / 32; ++cc)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              s[cc][j] = (cc * 32 + j <= limit) ? s[cc][j] : __float_as_uint(-INFINITY);
+        }
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int h = 0; h < BN / 64; ++h) {
-          uint32_t s[2][32];
-          tmem_ld_x32(tS + h * 64, s[0]);
-          tmem_ld_x32(tS + h * 64 + 32, s[1]);
-          tmem_wait_ld(s[0]);
-          tmem_wait_ld(s[1]);
+        for (int cc = 0; cc < BN / 32; ++cc)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int cc = j >> 4, jj = (j & 15) * 2;
-            float a = __uint_as_float(s[cc][jj]), b = __uint_as_float(s[cc][jj + 1]);
-            if (!full) {
-              const int c0 = h * 64 + 2 * j;
-              a = (c0 <= limit) ? a : -INFINITY;
-              b = (c0 + 1 <= limit) ? b : -INFINITY;
-            }
-            mx4[j & 3] = fmax3(mx4[j & 3], a, b);
-          }
-        }
+          for (int j = 0; j < 16; ++j)
+            mx4[j & 3] = fmax3(mx4[j & 3], __uint_as_float(s[cc][2 * j]), __uint_as_float(s[cc][2 * j + 1]));
         float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * sl2;
         float factor = 1.f;
         bool resc = false;
@@ -445,36 +454,27 @@ __global__ void __launch_bounds__(320, 1)
           resc = true;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, written over S.
-        // Packed f32x2 FMA for the exponent argument and packed adds (two
-        // independent accumulators each) for the fp32 and bf16 row sums.
+        // P = 2^(s*scale*log2e - m) as bf16 pairs, written over S. Packed f32x2
+        // FMA for the exponent argument and packed adds (two independent
+        // accumulators each) for the fp32 and bf16 row sums. Masked entries
+        // hold -inf and give exactly 0.
         const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
         uint64_t rs2[2] = {0ull, 0ull}, rt2[2] = {0ull, 0ull};
-#pragma unroll 1
-        for (int h = 0; h < BN / 64; ++h) {
-          uint32_t s[2][32];
-          tmem_ld_x32(tS + h * 64, s[0]);
-          tmem_ld_x32(tS + h * 64 + 32, s[1]);
-          tmem_wait_ld(s[0]);
-          tmem_wait_ld(s[1]);
-          uint32_t pk[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int cc = j >> 4, jj = (j & 15) * 2;
-            const int c0 = h * 64 + 2 * j;
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
             float e0, e1;
-            f2_unpack(ffma2(f2_pack(__uint_as_float(s[cc][jj]), __uint_as_float(s[cc][jj + 1])), sc2, nm2), e0, e1);
-            float p0 = fast_exp2(e0);
-            float p1 = fast_exp2(e1);
-            if (!full) {
-              p0 = (c0 <= limit) ? p0 : 0.f;
-              p1 = (c0 + 1 <= limit) ? p1 : 0.f;
-            }
+            f2_unpack(ffma2(f2_pack(__uint_as_float(s[cc][2 * j]), __uint_as_float(s[cc][2 * j + 1])), sc2, nm2),
+                      e0, e1);
+            const float p0 = fast_exp2(e0);
+            const float p1 = fast_exp2(e1);
             pk[j] = pack_bf16x2(p0, p1);
             rs2[j & 1] = fadd2(rs2[j & 1], f2_pack(p0, p1));
             rt2[j & 1] = fadd2(rt2[j & 1], f2_pack(__uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xFFFF0000u)));
           }
-          tmem_st_x32(tS + h * 32, pk);
+          tmem_st_x16(tS + cc * 16, pk);
         }
         float rs, rt;
         {

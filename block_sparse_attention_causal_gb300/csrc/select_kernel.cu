@@ -13,10 +13,10 @@
 //      of lane l is block 32*jj + l, so the ballot at step jj is word jj of
 //      the row's support bitmask (kept by lane jj). Steps are OR-ed, then the
 //      sink / diagonal blocks added.
-//  scan_rows_kernel   : exclusive scan of the row counts -> row_ptr, nnz.
-//  emit_rows_kernel   : bitmask -> ascending col_idx at row_ptr[row].
-//  order_units_kernel : late-step work order: per L2 group of (batch, head)
-//      slices, units sorted by number of listed blocks, heaviest first.
+//  finalize_kernel    : row_ptr (each CTA adds up the counts before its rows),
+//      nnz, ascending col_idx from the bitmasks, and the late-step work order:
+//      per L2 group of (batch, head) slices, units sorted by number of listed
+//      blocks, heaviest first.
 #include <stdint.h>
 
 #include "internal.h"
@@ -50,6 +50,15 @@ __device__ __forceinline__ int64_t warp_sum64(int64_t v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
+}
+// Warp sum of lane values in [0, 2^63 / 32): three 21-bit slices summed with
+// the hardware reduction (each slice sum < 2^26), then recombined exactly.
+__device__ __forceinline__ int64_t warp_sum_u63(int64_t v) {
+  const uint64_t u = static_cast<uint64_t>(v);
+  const uint32_t a = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(u & 0x1FFFFFu));
+  const uint32_t b = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>((u >> 21) & 0x1FFFFFu));
+  const uint32_t c = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(u >> 42));
+  return static_cast<int64_t>(a) + (static_cast<int64_t>(b) << 21) + (static_cast<int64_t>(c) << 42);
 }
 __device__ __forceinline__ int warp_sum32(int v) {
 #pragma unroll
@@ -102,7 +111,7 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
         int64_t sacc = 0;
 #pragma unroll
         for (int jj = 0; jj < NJ; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
-        sacc = warp_sum64(sacc);
+        sacc = warp_sum_u63(sacc);
         if (sacc >= p.target_fx) v = cand;
       }
       int64_t s_gt = 0;
@@ -145,78 +154,11 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
   if (lane == 0) p.counts[row] = cnt;
 }
 
-// Single CTA: exclusive scan of counts into row_ptr.
-__global__ void __launch_bounds__(1024) scan_rows_kernel(const SelectParams p) {
-  __shared__ int64_t warp_tot[32];
-  const int64_t rows = (int64_t)p.bh_count * p.nb;
-  const int tid = threadIdx.x;
-  const int64_t per = (rows + 1023) / 1024;
-  const int64_t r0 = min(rows, tid * per), r1 = min(rows, r0 + per);
-  int64_t local = 0;
-  for (int64_t r = r0; r < r1; ++r) local += p.counts[r];
-  // block-wide exclusive scan of `local`
-  const int lane = tid & 31, warp = tid >> 5;
-  int64_t inc = local;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += y;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int64_t t = warp_tot[lane];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, t, off);
-      if (lane >= off) t += y;
-    }
-    warp_tot[lane] = t;  // inclusive over warps
-  }
-  __syncthreads();
-  int64_t base = inc - local + (warp > 0 ? warp_tot[warp - 1] : 0);
-  for (int64_t r = r0; r < r1; ++r) {
-    p.row_ptr[r] = (int32_t)base;
-    base += p.counts[r];
-  }
-  if (tid == 1023) {
-    p.row_ptr[rows] = (int32_t)base;
-    if (p.nnz) *p.nnz = (int32_t)base;
-    if (base > p.col_cap) atomicOr(p.err, kErrBadSupport);
-  }
-}
+constexpr int kChunkRows = 256;  // rows per finalize CTA (one per thread)
 
-// One warp per row: write the set bits of the row's bitmask in ascending order.
-__global__ void __launch_bounds__(256) emit_rows_kernel(const SelectParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int64_t rows = (int64_t)p.bh_count * p.nb;
-  if (row >= rows) return;
-  const uint32_t word = (lane < p.nwords) ? p.bits[row * p.nwords + lane] : 0u;
-  const int c = __popc(word);
-  int excl = c;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, excl, off);
-    if (lane >= off) excl += y;
-  }
-  excl -= c;
-  const int64_t start = p.row_ptr[row];
-  if (start + p.counts[row] > p.col_cap) return;  // flagged by the scan
-  uint32_t w = word;
-  int64_t pos = start + excl;
-  while (w) {
-    const int bit = __ffs(w) - 1;
-    p.col_idx[pos++] = lane * 32 + bit;
-    w &= w - 1;
-  }
-}
-
-// One CTA per L2 group: rank units by cost (listed blocks), heaviest first,
-// ties by unit index.
-__global__ void __launch_bounds__(256) order_units_kernel(const SelectParams p) {
-  extern __shared__ int32_t cost[];
-  const int g = blockIdx.x;
+// Rank the units of one L2 group by cost (listed blocks), heaviest first, ties
+// by unit index, and write their global order.
+__device__ void order_group(const SelectParams& p, int g, int32_t* cost) {
   const int h0 = g * p.group_heads;
   const int gsize = min(p.group_heads, p.bh_count - h0);
   const int units = gsize * p.npairs;
@@ -238,8 +180,79 @@ __global__ void __launch_bounds__(256) order_units_kernel(const SelectParams p) 
       const int cv = cost[v];
       pos += (cv > c || (cv == c && v < u)) ? 1 : 0;
     }
-    const int bh = h0 + u / p.npairs, pr = u % p.npairs;
-    p.tile_order[gbase + pos] = bh * p.npairs + pr;
+    p.tile_order[gbase + pos] = h0 * p.npairs + u;
+  }
+}
+
+// Finalize, one launch: CTAs [0, n_chunks) each take kChunkRows rows, add up
+// the counts of every earlier row themselves (no separate scan pass), write
+// their row_ptr entries and emit their rows' column lists in ascending order;
+// the remaining CTAs build the late-step work order, one L2 group each.
+__global__ void __launch_bounds__(kChunkRows) finalize_kernel(const SelectParams p, int n_chunks) {
+  extern __shared__ int32_t sh[];
+  __shared__ int64_t red[kChunkRows / 32];
+  __shared__ int32_t start_s[kChunkRows];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if ((int)blockIdx.x >= n_chunks) {
+    order_group(p, blockIdx.x - n_chunks, sh);
+    return;
+  }
+  const int64_t rows = (int64_t)p.bh_count * p.nb;
+  const int64_t r0 = (int64_t)blockIdx.x * kChunkRows;
+  // counts of all rows before this chunk
+  int64_t pre = 0;
+  for (int64_t r = tid; r < r0; r += kChunkRows) pre += p.counts[r];
+  pre = warp_sum64(pre);
+  if (lane == 0) red[warp] = pre;
+  __syncthreads();
+  int64_t prefix = 0;
+#pragma unroll
+  for (int w = 0; w < kChunkRows / 32; ++w) prefix += red[w];
+  __syncthreads();
+  // exclusive scan of this chunk's counts
+  const int64_t r = r0 + tid;
+  const int c = (r < rows) ? p.counts[r] : 0;
+  int inc = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
+  }
+  if (lane == 31) red[warp] = inc;
+  __syncthreads();
+  int64_t wpre = 0;
+  for (int w = 0; w < warp; ++w) wpre += red[w];
+  const int64_t start = prefix + wpre + inc - c;
+  if (r < rows) p.row_ptr[r] = (int32_t)start;
+  start_s[tid] = (int32_t)start;
+  if (r == rows - 1) {
+    p.row_ptr[rows] = (int32_t)(start + c);
+    if (p.nnz) *p.nnz = (int32_t)(start + c);
+    if (start + c > p.col_cap) atomicOr(p.err, kErrBadSupport);
+  }
+  __syncthreads();
+  // emit: one warp per row, lane j holds bitmask word j
+  for (int i = warp; i < kChunkRows; i += kChunkRows / 32) {
+    const int64_t row = r0 + i;
+    if (row >= rows) break;
+    const uint32_t word = (lane < p.nwords) ? p.bits[row * p.nwords + lane] : 0u;
+    const int wc = __popc(word);
+    int excl = wc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, excl, off);
+      if (lane >= off) excl += y;
+    }
+    excl -= wc;
+    const int64_t st = start_s[i];
+    if (st + p.counts[row] > p.col_cap) continue;  // flagged above
+    uint32_t w = word;
+    int64_t pos = st + excl;
+    while (w) {
+      const int bit = __ffs(w) - 1;
+      p.col_idx[pos++] = lane * 32 + bit;
+      w &= w - 1;
+    }
   }
 }
 
@@ -273,17 +286,14 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   else if (rounds <= 8) select_rows_kernel<8><<<grid_rows, 256, 0, stream>>>(p);
   else if (rounds <= 16) select_rows_kernel<16><<<grid_rows, 256, 0, stream>>>(p);
   else select_rows_kernel<32><<<grid_rows, 256, 0, stream>>>(p);
-  scan_rows_kernel<<<1, 1024, 0, stream>>>(p);
-  emit_rows_kernel<<<grid_rows, 256, 0, stream>>>(p);
-  if (s.tile_order) {
-    const int groups = (s.bh_count + s.group_heads - 1) / s.group_heads;
-    const size_t shm = (size_t)s.group_heads * s.npairs * sizeof(int32_t);
-    if (shm > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(order_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
-      if (e != cudaSuccess) return e;
-    }
-    order_units_kernel<<<groups, 256, shm, stream>>>(p);
+  const int n_chunks = (int)((rows + kChunkRows - 1) / kChunkRows);
+  const int groups = s.tile_order ? (s.bh_count + s.group_heads - 1) / s.group_heads : 0;
+  const size_t shm = s.tile_order ? (size_t)s.group_heads * s.npairs * sizeof(int32_t) : 0;
+  if (shm > 40 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
+    if (e != cudaSuccess) return e;
   }
+  finalize_kernel<<<n_chunks + groups, kChunkRows, shm, stream>>>(p, n_chunks);
   return cudaGetLastError();
 }
 

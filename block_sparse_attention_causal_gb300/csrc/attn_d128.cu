@@ -1,4 +1,6 @@
 // Instantiations of the tcgen05 attention kernel for head_dim = 128.
+#include <atomic>
+
 #include "attn_kernel.cuh"
 
 namespace wise {
@@ -6,18 +8,28 @@ namespace {
 
 template <int D, int BN, bool SPARSE>
 cudaError_t launch_one(const CUtensorMap* m, const AttnParams& p, cudaStream_t st) {
-  using C = AttnCfg<D, BN>;
+  using C = AttnCfg<D, BN, SPARSE>;
   static bool configured[64] = {};
+  static int sm_count[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
     e = cudaFuncSetAttribute(wise_attn_kernel<D, BN, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
   }
-  wise_attn_kernel<D, BN, SPARSE><<<(unsigned)p.n_units, C::THREADS, C::SMEM_BYTES, st>>>(m[0], m[1], m[2], p);
+  // persistent: one CTA per SM (the shared-memory footprint allows no more);
+  // each launch takes the next work-counter slot
+  static std::atomic<uint32_t> launches{0};
+  AttnParams q = p;
+  q.sched_slot = launches.fetch_add(1u) % kSchedSlots;
+  const int64_t grid = p.n_units < sm_count[dev] ? p.n_units : sm_count[dev];
+  wise_attn_kernel<D, BN, SPARSE><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(m[0], m[1], m[2], q);
   return cudaGetLastError();
 }
 

@@ -7,8 +7,10 @@
 //  * reuse    (SPARSE = true): attention restricted to the CSR block support,
 //    §5.2 Eqs 7-8 -- only listed key blocks are loaded and multiplied.
 //
-// One CTA = one work unit = two 128-row query tiles ("streams") of one
-// (batch, head). Warp roles (384 threads, three warpgroups):
+// Persistent: one CTA per SM pulls work units (two 128-row query tiles,
+// "streams", of one (batch, head)) from the work order, heaviest first. While one unit's epilogue
+// runs, the next unit's Q/K/V loads and first MMAs proceed. Warp roles (384
+// threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles once, then K/V blocks into an NST ring
 //   warp 1      TMEM allocator + MMA issuer (single thread)
 //   warps 2-3   idle (the control warpgroup gives its registers away)
@@ -31,7 +33,17 @@
 
 namespace wise {
 
-template <int D, int BN>
+// Work counters of the persistent kernels: each launch takes one slot of this
+// ring (chosen by the host launcher), its CTAs pull work units from `next`
+// with atomics, and the last CTA to finish resets the slot for a later launch.
+struct SchedSlot {
+  unsigned int next;
+  unsigned int done;
+};
+constexpr int kSchedSlots = 256;
+static __device__ SchedSlot g_sched[kSchedSlots];
+
+template <int D, int BN, bool SPARSE>
 struct AttnCfg {
   static_assert(D == 64 || D == 96 || D == 128, "head_dim");
   static_assert(BN == 64 || BN == 128, "block");
@@ -42,7 +54,10 @@ struct AttnCfg {
   static constexpr uint32_t Q_BYTES = 128u * D * 2u;
   static constexpr uint32_t KV_BYTES = (uint32_t)BN * D * 2u;
   static constexpr uint32_t SMEM_BUDGET = 230400u;
-  static constexpr int NST_FIT = (int)((SMEM_BUDGET - 2u * Q_BYTES) / (2u * KV_BYTES));
+  static constexpr int MAX_NB = 1024;
+  // per-warp partial block masses of the Eq 5 epilogue, [2 streams][4 warps][nb]
+  static constexpr uint32_t PART_BYTES = SPARSE ? 0u : 2u * 4u * MAX_NB * 4u;
+  static constexpr int NST_FIT = (int)((SMEM_BUDGET - 2u * Q_BYTES - PART_BYTES) / (2u * KV_BYTES));
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;  // K/V ring depth
   static_assert(NST >= 2, "ring");
   static constexpr int THREADS = 384;
@@ -53,11 +68,14 @@ struct AttnCfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2u * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + NST * KV_BYTES;
+  static constexpr uint32_t OFF_PART = OFF_V + NST * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_PART + PART_BYTES;
+  static constexpr int RING = 4;  // work units published to the consumer roles
   // q_full[2] k_full[NST] v_full[NST] kv_empty[NST] s_full[2] p_full[2] o_final[2] drain
-  static constexpr int NBAR = 2 + 3 * NST + 2 + 2 + 2 + 1;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16u + 1024u;  // + alignment slack
+  // ring_full[RING] ring_empty[RING]
+  static constexpr int NBAR = 2 + 3 * NST + 2 + 2 + 2 + 1 + 2 * RING;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;  // tmem base, abort flag, ring of unit ids
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16u + 4u * RING + 1024u;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns: S/P of stream i at s_col(i), O of stream i at o_col(i)
   __host__ __device__ static constexpr uint32_t s_col(int i) { return i ? 128u : 0u; }
@@ -190,7 +208,7 @@ template <int D, int BN, bool SPARSE>
 __global__ void __launch_bounds__(384, 1)
     wise_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-  using C = AttnCfg<D, BN>;
+  using C = AttnCfg<D, BN, SPARSE>;
   constexpr int NST = C::NST;
   constexpr uint32_t ROWB = C::ROWB;
   extern __shared__ uint8_t smem_raw[];
@@ -205,23 +223,12 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_final = p_full + 2;
   uint64_t* drain = o_final + 2;
+  uint64_t* ring_full = drain + 1;
+  uint64_t* ring_empty = ring_full + C::RING;
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
 
-  int64_t unit;
-  if (SPARSE && p.tile_order != nullptr) {
-    unit = __ldg(p.tile_order + blockIdx.x);
-  } else {
-    unit = default_unit(blockIdx.x, p);
-  }
-  if (unit < 0 || unit >= p.n_units) {  // malformed schedule: whole CTA leaves before any setup
-    if (threadIdx.x == 0) atomicOr(p.err, kErrBadSupport);
-    return;
-  }
-  const int bh = (int)(unit / p.npairs);
-  const int pair = (int)(unit % p.npairs);
-  const int tile[2] = {2 * pair, 2 * pair + 1};
-  const bool has1 = tile[1] < p.n_qtiles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -238,6 +245,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&o_final[i], 1);
     }
     mbar_init(drain, 1);
+    for (int j = 0; j < C::RING; ++j) {
+      mbar_init(&ring_full[j], 1);
+      mbar_init(&ring_empty[j], 1 + 256);  // MMA thread + both softmax warpgroups
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -250,13 +261,40 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_base_slot;
 
-  auto make_cursor = [&](TileCursor& c, int i) {
-    if (i == 1 && !has1) {
+  // Work distribution: the producer thread pulls positions x of the work
+  // order from the launch's counter (greedy, heaviest units first) and
+  // publishes the unit ids through a shared-memory ring; every other role
+  // reads the same sequence from the ring. -1 ends the sequence, -2 marks a
+  // malformed schedule entry (skipped).
+  struct Unit {
+    int bh, tile[2];
+    bool has1;
+  };
+  auto decode = [&](int id, Unit& u) {
+    u.bh = id / p.npairs;
+    const int pair = id % p.npairs;
+    u.tile[0] = 2 * pair;
+    u.tile[1] = 2 * pair + 1;
+    u.has1 = u.tile[1] < p.n_qtiles;
+  };
+  // consumer side: next unit id from the ring (-1 at the end or on abort)
+  auto ring_take = [&](int& ci, bool warp_vote) -> int {
+    const int slot = ci % C::RING;
+    bool okw = mbar_wait(&ring_full[slot], (ci / C::RING) & 1, abort_flag, p.err);
+    if (warp_vote) okw = __all_sync(0xffffffffu, okw);
+    if (!okw) return -1;
+    const int id = ring[slot];
+    mbar_arrive(&ring_empty[slot]);
+    ++ci;
+    return id;
+  };
+  auto make_cursor = [&](TileCursor& c, const Unit& u, int i) {
+    if (i == 1 && !u.has1) {
       c.init_empty();
     } else if (SPARSE) {
-      c.init_sparse(tile[i], bh, p, C::ENT_PER_TILE);
+      c.init_sparse(u.tile[i], u.bh, p, C::ENT_PER_TILE);
     } else {
-      c.init_dense(tile[i], p, BN);
+      c.init_dense(u.tile[i], p, BN);
     }
   };
 
@@ -268,32 +306,55 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      for (int i = 0; i < (has1 ? 2 : 1); ++i) {
-        const int row = bh * p.n + tile[i] * 128;
-        mbar_arrive_expect_tx(&q_full[i], C::Q_BYTES);
-        for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ[i] + c * 128 * ROWB, &tm_q, &q_full[i], c * C::CH, row);
+      uint32_t nq[2] = {0u, 0u};  // Q loads per stream (one per unit using it)
+      int k = 0;                  // K/V loads issued (ring position)
+      bool ok = true;
+      SchedSlot* sched = &g_sched[p.sched_slot];
+      for (int pi = 0; ok; ++pi) {
+        const int slot = pi % C::RING;
+        if (pi >= C::RING && !(ok = mbar_wait(&ring_empty[slot], ((pi / C::RING) - 1) & 1, abort_flag, p.err)))
+          break;
+        const unsigned int x = atomicAdd(&sched->next, 1u);
+        int id = -1;
+        if ((int64_t)x < p.n_units) {
+          const int64_t v = (SPARSE && p.tile_order != nullptr) ? (int64_t)__ldg(p.tile_order + x) : default_unit(x, p);
+          id = (v >= 0 && v < p.n_units) ? (int)v : -2;
+          if (id == -2) atomicOr(p.err, kErrBadSupport);
+        }
+        ring[slot] = id;
+        mbar_arrive(&ring_full[slot]);
+        if (id == -1) break;
+        if (id < 0) continue;
+        Unit u;
+        decode(id, u);
+        for (int i = 0; i < (u.has1 ? 2 : 1) && ok; ++i) {
+          // the previous unit that used Q_i has finished all its MMAs
+          if (nq[i] > 0 && !(ok = mbar_wait(&o_final[i], (nq[i] - 1) & 1, abort_flag, p.err))) break;
+          const int row = u.bh * p.n + u.tile[i] * 128;
+          mbar_arrive_expect_tx(&q_full[i], C::Q_BYTES);
+          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ[i] + c * 128 * ROWB, &tm_q, &q_full[i], c * C::CH, row);
+          ++nq[i];
+        }
+        PairCursor pc;
+        make_cursor(pc.c[0], u, 0);
+        make_cursor(pc.c[1], u, 1);
+        pc.start();
+        int32_t blk;
+        uint32_t who;
+        while (ok && pc.next(blk, who)) {
+          const int s = k % NST;
+          if (k >= NST && !(ok = mbar_wait(&kv_empty[s], ((k / NST) - 1) & 1, abort_flag, p.err))) break;
+          const int row = u.bh * p.n + blk * BN;
+          uint8_t* sk = smem + C::OFF_K + s * C::KV_BYTES;
+          uint8_t* sv = smem + C::OFF_V + s * C::KV_BYTES;
+          mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
+          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sk + c * BN * ROWB, &tm_k, &k_full[s], c * C::CH, row);
+          mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
+          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sv + c * BN * ROWB, &tm_v, &v_full[s], c * C::CH, row);
+          ++k;
+        }
+        if (pc.c[0].bad || pc.c[1].bad) atomicOr(p.err, kErrBadSupport);
       }
-      PairCursor pc;
-      make_cursor(pc.c[0], 0);
-      make_cursor(pc.c[1], 1);
-      if (pc.c[0].bad || pc.c[1].bad) atomicOr(p.err, kErrBadSupport);
-      pc.start();
-      int k = 0;
-      int32_t blk;
-      uint32_t who;
-      while (pc.next(blk, who)) {
-        const int s = k % NST;
-        if (k >= NST && !mbar_wait(&kv_empty[s], ((k / NST) - 1) & 1, abort_flag, p.err)) break;
-        const int row = bh * p.n + blk * BN;
-        uint8_t* sk = smem + C::OFF_K + s * C::KV_BYTES;
-        uint8_t* sv = smem + C::OFF_V + s * C::KV_BYTES;
-        mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
-        for (int c = 0; c < C::NCH; ++c) tma_load_2d(sk + c * BN * ROWB, &tm_k, &k_full[s], c * C::CH, row);
-        mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
-        for (int c = 0; c < C::NCH; ++c) tma_load_2d(sv + c * BN * ROWB, &tm_v, &v_full[s], c * C::CH, row);
-        ++k;
-      }
-      if (pc.c[0].bad || pc.c[1].bad) atomicOr(p.err, kErrBadSupport);
       // No copy into this CTA's shared memory may outlive the CTA.
       for (int j = (k > NST ? k - NST : 0); j < k; ++j) {
         const int s = j % NST;
@@ -301,8 +362,8 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait_drain(&k_full[s], ph, p.err);
         mbar_wait_drain(&v_full[s], ph, p.err);
       }
-      mbar_wait_drain(&q_full[0], 0, p.err);
-      if (has1) mbar_wait_drain(&q_full[1], 0, p.err);
+      for (int i = 0; i < 2; ++i)
+        if (nq[i] > 0) mbar_wait_drain(&q_full[i], (nq[i] - 1) & 1, p.err);
     }
     __syncwarp();
    } else if (warp == 1) {
@@ -310,21 +371,19 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
       constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
-      PairCursor pc;
-      make_cursor(pc.c[0], 0);
-      make_cursor(pc.c[1], 1);
-      pc.start();
       bool ok = true;
-      bool q_ready[2] = {false, false};
+      uint32_t nq[2] = {0u, 0u};    // units seen per stream (q_full / o_final phases)
+      uint32_t n_pt[2] = {0u, 0u};  // P tiles consumed per stream (p_full phases)
+      uint32_t n_pv[2] = {0u, 0u};  // PV MMAs in the current unit (accumulate flag)
       bool pending[2] = {false, false};
       int pend_slot[2] = {0, 0};
       uint32_t pend_ph[2] = {0, 0};
-      uint32_t n_pv[2] = {0, 0};
       uint32_t rem[NST];
       for (int s = 0; s < NST; ++s) rem[s] = 0;
 
       auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i], n_pv[i] & 1, abort_flag, p.err)) return false;
+        if (!mbar_wait(&p_full[i], n_pt[i] & 1, abort_flag, p.err)) return false;
+        ++n_pt[i];
         const int s = pend_slot[i];
         if (!mbar_wait(&v_full[s], pend_ph[i], abort_flag, p.err)) return false;
         tc_fence_after();
@@ -341,45 +400,65 @@ __global__ void __launch_bounds__(384, 1)
       };
 
       int k = 0;
-      int32_t blk;
-      uint32_t who;
-      while (ok && pc.next(blk, who)) {
-        const int s = k % NST;
-        const uint32_t ph = (k / NST) & 1;
-        bool k_ready = false;
-        rem[s] = __popc(who);
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (pending[i] && !(ok = issue_pv(i))) break;
-          if (!(who & (1u << i))) continue;
-          if (!q_ready[i]) {
-            if (!(ok = mbar_wait(&q_full[i], 0, abort_flag, p.err))) break;
-            q_ready[i] = true;
-          }
-          if (!k_ready) {
-            if (!(ok = mbar_wait(&k_full[s], ph, abort_flag, p.err))) break;
-            k_ready = true;
-          }
-          tc_fence_after();
-          const uint32_t qa = smem_u32(sQ[i]);
-          const uint32_t ka = smem_u32(smem + C::OFF_K + s * C::KV_BYTES);
+      int ci = 0;
+      while (ok) {
+        const int id = ring_take(ci, false);
+        if (id == -1) break;
+        if (id < 0) continue;
+        Unit u;
+        decode(id, u);
+        PairCursor pc;
+        make_cursor(pc.c[0], u, 0);
+        make_cursor(pc.c[1], u, 1);
+        pc.start();
+        bool q_ready[2] = {false, false};
+        n_pv[0] = n_pv[1] = 0;
+        int32_t blk;
+        uint32_t who;
+        while (ok && pc.next(blk, who)) {
+          const int s = k % NST;
+          const uint32_t ph = (k / NST) & 1;
+          bool k_ready = false;
+          rem[s] = __popc(who);
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (pending[i] && !(ok = issue_pv(i))) break;
+            if (!(who & (1u << i))) continue;
+            if (!q_ready[i]) {
+              if (!(ok = mbar_wait(&q_full[i], nq[i] & 1, abort_flag, p.err))) break;
+              q_ready[i] = true;
+            }
+            if (!k_ready) {
+              if (!(ok = mbar_wait(&k_full[s], ph, abort_flag, p.err))) break;
+              k_ready = true;
+            }
+            tc_fence_after();
+            const uint32_t qa = smem_u32(sQ[i]);
+            const uint32_t ka = smem_u32(smem + C::OFF_K + s * C::KV_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int c = kk / (C::CH / 16), w = kk % (C::CH / 16);
-            const uint64_t adesc = smem_desc(qa + c * 128 * ROWB + w * 32, 16, 8 * ROWB, C::SWZ);
-            const uint64_t bdesc = smem_desc(ka + c * BN * ROWB + w * 32, 16, 8 * ROWB, C::SWZ);
-            umma_ss(tbase + C::s_col(i), adesc, bdesc, IDESC_S, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int c = kk / (C::CH / 16), w = kk % (C::CH / 16);
+              const uint64_t adesc = smem_desc(qa + c * 128 * ROWB + w * 32, 16, 8 * ROWB, C::SWZ);
+              const uint64_t bdesc = smem_desc(ka + c * BN * ROWB + w * 32, 16, 8 * ROWB, C::SWZ);
+              umma_ss(tbase + C::s_col(i), adesc, bdesc, IDESC_S, kk > 0);
+            }
+            umma_commit(&s_full[i]);
+            pending[i] = true;
+            pend_slot[i] = s;
+            pend_ph[i] = ph;
           }
-          umma_commit(&s_full[i]);
-          pending[i] = true;
-          pend_slot[i] = s;
-          pend_ph[i] = ph;
+          ++k;
         }
-        ++k;
+        for (int i = 0; i < 2 && ok; ++i)
+          if (pending[i]) ok = issue_pv(i);
+        // Close the unit for each stream it uses: its Q load has landed (so the
+        // next load into that buffer cannot overlap it) and o_final fires once
+        // every MMA issued so far has completed.
+        for (int i = 0; i < (u.has1 ? 2 : 1) && ok; ++i) {
+          if (!q_ready[i]) ok = mbar_wait(&q_full[i], nq[i] & 1, abort_flag, p.err);
+          umma_commit(&o_final[i]);
+          ++nq[i];
+        }
       }
-      for (int i = 0; i < 2 && ok; ++i)
-        if (pending[i]) ok = issue_pv(i);
-      for (int i = 0; i < 2; ++i)
-        if (n_pv[i] > 0) umma_commit(&o_final[i]);
       umma_commit(drain);  // every MMA of this CTA done before TMEM is released
       mbar_wait_drain(drain, 0, p.err);
     }
@@ -391,32 +470,44 @@ __global__ void __launch_bounds__(384, 1)
     const int i = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
-    if (!(i == 1 && !has1)) {
-      const int t = tile[i];
+    const uint32_t trow = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = trow + C::s_col(i);
+    const uint32_t tO = trow + C::o_col(i);
+    const float sl2 = p.scale_log2;
+    const bool want_mass = (!SPARSE) && (p.mass != nullptr);
+    const int half = (BN == 64) ? (r >> 6) : 0;
+    float* part = reinterpret_cast<float*>(smem + C::OFF_PART) + i * 4 * C::MAX_NB;
+    uint32_t n_s = 0;   // S tiles consumed (s_full phases)
+    uint32_t nq = 0;    // units processed (o_final phases)
+    bool ok = true;
+    int ci = 0;
+    while (ok) {
+      const int id = ring_take(ci, true);
+      if (id == -1) break;
+      if (id < 0) continue;
+      Unit u;
+      decode(id, u);
+      if (i == 1 && !u.has1) continue;
+      const int bh = u.bh;
+      const int t = u.tile[i];
       const int qpos = t * 128 + r;
       const bool row_valid = qpos < p.n;
-      const uint32_t trow = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-      const uint32_t tS = trow + C::s_col(i);
-      const uint32_t tO = trow + C::o_col(i);
-      const float sl2 = p.scale_log2;
-      const bool want_mass = (!SPARSE) && (p.mass != nullptr);
       float* lam = want_mass ? p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + r : nullptr;
-      const int half = (BN == 64) ? (r >> 6) : 0;
 
       TileCursor cur;
-      make_cursor(cur, i);
+      make_cursor(cur, u, i);
       // l: fp32 row sum (for LSE and the block masses); lt: sum of the
       // bf16-rounded P that the tensor core multiplies (normalises O, so the
       // output is an exact weighted mean of the rounded weights)
       float m_ref = -INFINITY, l = 0.f, lt = 0.f;
       uint32_t cnt = 0;
-      bool ok = true;
       int32_t blk;
       uint32_t mask;
       while (cur.next(blk, mask)) {
-        ok = mbar_wait(&s_full[i], cnt & 1, abort_flag, p.err);
+        ok = mbar_wait(&s_full[i], n_s & 1, abort_flag, p.err);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        ++n_s;
         tc_fence_after();
         const int kbase = blk * BN;
         const bool row_on = (mask >> half) & 1u;
@@ -505,9 +596,10 @@ __global__ void __launch_bounds__(384, 1)
       }
 
       // ------------------------------------------------------------ epilogue
-      if (ok && cnt > 0) {
-        ok = mbar_wait(&o_final[i], 0, abort_flag, p.err);
+      if (ok) {  // the unit's MMAs are complete (waited even without entries: keeps phases in step)
+        ok = mbar_wait(&o_final[i], nq & 1, abort_flag, p.err);
         ok = __all_sync(0xffffffffu, ok);
+        ++nq;
         tc_fence_after();
       }
       if (ok) {
@@ -549,7 +641,6 @@ __global__ void __launch_bounds__(384, 1)
         if (p.lse != nullptr && row_valid) p.lse[grow] = lse2 * 0.69314718055994531f;
         if (want_mass) {
           // Eq 5: r_qb = (1/B) sum over the block's rows of 2^(lam_ib - lse2_i).
-          float* part = reinterpret_cast<float*>(sQ[i]);  // Q tile is dead once o_final fired
 #pragma unroll 1
           for (uint32_t e = 0; e < cnt; ++e) {
             float a = (row_valid && l > 0.f) ? fast_exp2(lam[(size_t)e * 128] - lse2) : 0.f;
@@ -576,6 +667,7 @@ __global__ void __launch_bounds__(384, 1)
               dst[e] = v;
             }
           }
+          named_bar_sync(1 + i, 128);  // partials are reused by the next unit
         }
       }
     }
@@ -586,6 +678,15 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    // every CTA has pulled its last position: the last one out resets the slot
+    __threadfence();
+    if (atomicAdd(&g_sched[p.sched_slot].done, 1u) == gridDim.x - 1) {
+      g_sched[p.sched_slot].next = 0u;
+      g_sched[p.sched_slot].done = 0u;
+      __threadfence();
+    }
   }
 }
 

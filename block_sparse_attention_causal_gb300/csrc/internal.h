@@ -25,6 +25,7 @@ struct AttnParams {
   const int32_t* tile_order;  // optional unit order (reuse only)
   int64_t n_units;
   uint32_t* err;
+  uint32_t sched_slot;  // work-counter slot of this launch
 };
 
 struct SelectLaunch {

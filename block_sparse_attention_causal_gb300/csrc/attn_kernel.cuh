@@ -241,13 +241,13 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 4);  // one elected arrival per softmax warp
       mbar_init(&o_final[i], 1);
     }
     mbar_init(drain, 1);
     for (int j = 0; j < C::RING; ++j) {
       mbar_init(&ring_full[j], 1);
-      mbar_init(&ring_empty[j], 1 + 256);  // MMA thread + both softmax warpgroups
+      mbar_init(&ring_empty[j], 1 + 8);  // MMA thread + one arrival per softmax warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -284,7 +284,12 @@ __global__ void __launch_bounds__(384, 1)
     if (warp_vote) okw = __all_sync(0xffffffffu, okw);
     if (!okw) return -1;
     const int id = ring[slot];
-    mbar_arrive(&ring_empty[slot]);
+    if (warp_vote) {
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&ring_empty[slot]);
+    } else {
+      mbar_arrive(&ring_empty[slot]);
+    }
     ++ci;
     return id;
   };
@@ -591,7 +596,8 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_st();
         if (want_mass) lam[(size_t)cnt * 128] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
         tc_fence_before();
-        mbar_arrive(&p_full[i]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[i]);
         ++cnt;
       }
 

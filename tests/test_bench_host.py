@@ -1,0 +1,55 @@
+"""Host-side logic of the benchmark: FLOP counting and the multi-rank
+aggregation (two gloo ranks on CPU)."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_support_flops_counts_admissible_pairs():
+    # nb = 3, block 4, one head: rows {0}, {0,1}, {1,2}
+    rp = np.array([0, 1, 3, 5], np.int32)
+    ci = np.array([0, 0, 1, 1, 2], np.int32)
+    d, blk = 8, 4
+    brute = 0
+    rows = [[0], [0, 1], [1, 2]]
+    for q, row in enumerate(rows):
+        for i in range(q * blk, (q + 1) * blk):
+            for b in row:
+                brute += sum(1 for j in range(b * blk, (b + 1) * blk) if j <= i)
+    assert bench.support_flops(rp, ci, 3, blk, d) == 4.0 * d * brute
+
+
+def test_whole_job_value_is_weak_scaling():
+    assert bench.whole_job_tflops(2e12, 1000.0, 1) == pytest.approx(2.0)
+    assert bench.whole_job_tflops(2e12, 1000.0, 4) == pytest.approx(8.0)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    vals = bench.reduce_max_over_ranks([1.0 + rank, 5.0 - rank, 2.0], world)
+    out[rank] = vals
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    world = 2
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, join=True, start_method="spawn")
+    assert out[0] == [2.0, 5.0, 2.0] and out[1] == [2.0, 5.0, 2.0]

@@ -30,7 +30,7 @@ WISE_SUPPORT_DIAG = 2
 EXPORTS = (
     "wise_abi_version", "wise_status_str", "wise_attn_discover_workspace", "wise_attn_discover",
     "wise_schedule_units", "wise_support_capacity", "wise_select_workspace", "wise_select_support",
-    "wise_attn_sparse", "wise_validate_support", "wise_device_status",
+    "wise_attn_sparse", "wise_validate_support", "wise_device_status", "wise_select_support_noalloc",
 )
 
 
@@ -72,6 +72,8 @@ _SIGNATURES = {
     "wise_select_workspace": (_sz, [_dp, _i32]),
     "wise_select_support": (ctypes.c_int, [_dp, _vp, _i32, ctypes.c_double, _u32, _vp, _vp, _i64, _vp, _vp, _vp,
                                            _sz, _vp]),
+    "wise_select_support_noalloc": (ctypes.c_int, [_dp, _vp, _i32, ctypes.c_double, _u32, _vp, _vp, _i64, _vp,
+                                                   _vp, _vp]),
     "wise_attn_sparse": (ctypes.c_int, [_dp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "wise_validate_support": (ctypes.c_int, [_dp, _vp, _vp, _u32]),
     "wise_device_status": (ctypes.c_int, [_vp]),

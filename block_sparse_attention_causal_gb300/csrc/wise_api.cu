@@ -166,6 +166,29 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
 
 int64_t fixed_point(double x) { return llrint(x * 4503599627370496.0); }  // x * 2^52, nearest even
 
+// Fixed scratch of wise_select_support_noalloc: the per-row support bitmasks
+// and counts that wise_select_support keeps in its caller's workspace. It is
+// part of the library image, so every GPU that loads the library holds these
+// bytes until the process exits; calls share it.
+constexpr size_t kNoAllocScratchBytes = 2u << 20;
+static __device__ __align__(256) uint8_t g_select_scratch[kNoAllocScratchBytes];
+uint8_t* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_select_scratch on the current device. The name is only
+// a host-side stand-in, so the address is looked up once per device (with that
+// device current) and cached.
+uint8_t* select_scratch() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  return g_scratch_ptr[dev];
+}
+
 }  // namespace
 }  // namespace wise
 
@@ -273,6 +296,49 @@ int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int
   sl.flags = flags;
   sl.bits = static_cast<uint32_t*>(workspace);
   sl.counts = reinterpret_cast<int32_t*>(static_cast<uint32_t*>(workspace) + rows * words);
+  sl.row_ptr = row_ptr;
+  sl.col_idx = col_idx;
+  sl.col_cap = col_capacity;
+  sl.nnz = nnz;
+  sl.tile_order = tile_order;
+  sl.npairs = s.npairs;
+  sl.qb_per_unit = 256 / s.bn;
+  sl.group_heads = s.group_heads;
+  sl.err = err;
+  cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
+}
+
+int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_mass, int32_t window, double eta,
+                                uint32_t flags, int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity,
+                                int32_t* tile_order, int32_t* nnz, wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!block_mass || !row_ptr || !col_idx) return WISE_ERR_INVALID_ARGUMENT;
+  if (window < 1 || window > 8 || !(eta > 0.0 && eta < 1.0) || (flags & ~3u)) return WISE_ERR_INVALID_ARGUMENT;
+  if (col_capacity < wise_support_capacity(desc)) return WISE_ERR_BAD_SUPPORT;
+  if (wise_select_workspace(desc, window) > kNoAllocScratchBytes) return WISE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(block_mass) & 3u) || (reinterpret_cast<uintptr_t>(row_ptr) & 3u) ||
+      (reinterpret_cast<uintptr_t>(col_idx) & 3u))
+    return WISE_ERR_ALIGNMENT;
+  uint32_t* err = error_word();
+  uint8_t* scratch = select_scratch();
+  if (!err || !scratch) return WISE_ERR_CUDA;
+  const Shape s = shape_of(desc);
+  const int64_t rows = s.bh * s.nb;
+  const int64_t words = (s.nb + 31) / 32;
+  SelectLaunch sl;
+  sl.mass = block_mass;
+  sl.window = window;
+  sl.bh_count = (int32_t)s.bh;
+  sl.nb = s.nb;
+  sl.target_fx = fixed_point(eta);
+  sl.tol_fx = fixed_point(1e-6);
+  sl.flags = flags;
+  // every row writes its bitmask words and its count before they are read,
+  // so the shared scratch needs no clearing between calls
+  sl.bits = reinterpret_cast<uint32_t*>(scratch);
+  sl.counts = reinterpret_cast<int32_t*>(scratch + rows * words * 4);
   sl.row_ptr = row_ptr;
   sl.col_idx = col_idx;
   sl.col_cap = col_capacity;

@@ -153,6 +153,36 @@ int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int
                         void* workspace, size_t workspace_bytes, wise_stream_t stream);
 
 /*
+ * wise_select_support_noalloc -- wise_select_support for callers that cannot
+ * allocate device memory. (Not an operation of the paper: the same selection
+ * as wise_select_support, only the scratch memory comes from elsewhere.)
+ * Some callers cannot call cudaMalloc or hand out a workspace: code running
+ * while a CUDA graph is being captured (allocation is not allowed there),
+ * engines whose memory plan is fixed before they run, or runtimes that own
+ * every byte of device memory through their own pool. This variant takes the
+ * same arguments minus the workspace and uses a 2 MiB scratch array that is
+ * part of the library image instead, so it allocates nothing.
+ *   - The scratch is held by every GPU that loads the library until the
+ *     process exits; shapes needing more than 2 MiB of selection workspace
+ *     (wise_select_workspace(desc, window) > 2 MiB: about 8 bytes per
+ *     (batch, head, query block) row plus 4 bytes per 32 key blocks, i.e.
+ *     up to ~260 000 rows when seq_len / block <= 32 and ~58 000 rows at
+ *     seq_len / block = 256) return WISE_ERR_WORKSPACE without launching.
+ *   - The first call on a device looks up the scratch address for that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture on the device.
+ *   - All calls share the one scratch array, which keeps the last call's
+ *     contents (nothing in it needs to start at zero): calls whose kernels
+ *     overlap on the GPU (different streams without ordering) race on it and
+ *     must be serialised by the caller.
+ * Arguments, outputs and status codes are those of wise_select_support.
+ */
+int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_mass, int32_t window,
+                                double eta, uint32_t flags, int32_t* row_ptr, int32_t* col_idx,
+                                int64_t col_capacity, int32_t* tile_order, int32_t* nnz,
+                                wise_stream_t stream);
+
+/*
  * wise_attn_sparse -- one late (reuse) recurrent step, §5.2 Eq 8:
  * O = softmax(Q K^T * scale + M + R) V where R is 0 on the key blocks listed
  * for the query's block and -inf elsewhere (Eq 7); M is causal. Only the

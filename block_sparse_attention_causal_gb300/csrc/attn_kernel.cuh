@@ -12,14 +12,15 @@
 // runs, the next unit's Q/K/V loads and first MMAs proceed. Warp roles (384
 // threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles once, then K/V blocks into an NST ring
-//   warp 1      TMEM allocator + MMA issuer (single thread)
-//   warps 2-3   idle (the control warpgroup gives its registers away)
+//   warp 1      TMEM allocator + MMA issuer of stream 0 (single thread)
+//   warp 2      MMA issuer of stream 1 (single thread)
+//   warp 3      idle (the control warpgroup gives its registers away)
 //   warps 4-7   softmax warpgroup of stream 0 (one query row per thread)
 //   warps 8-11  softmax warpgroup of stream 1
 // Registers are moved from the control warpgroup (96 each) to the softmax
 // warpgroups (200 each): 128*96 + 256*200 <= 384*168, the launch allocation.
-// The MMA thread walks the ascending union of both streams' key-block lists;
-// a K/V block read by both streams is loaded once. Per stream, S = Q K^T goes
+// Both MMA threads walk the ascending union of the two streams' key-block
+// lists; a K/V block read by both streams is loaded once. Per stream, S = Q K^T goes
 // to its own TMEM columns; the softmax warps turn S into P (bf16, written
 // back over S) and the MMA thread accumulates O += P V from TMEM. While one
 // stream's warps run the softmax, the tensor core works on the other stream.
@@ -71,9 +72,9 @@ struct AttnCfg {
   static constexpr uint32_t OFF_PART = OFF_V + NST * KV_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_PART + PART_BYTES;
   static constexpr int RING = 4;  // work units published to the consumer roles
-  // q_full[2] k_full[NST] v_full[NST] kv_empty[NST] s_full[2] p_full[2] o_final[2] drain
+  // q_full[2] kv_full[NST] kv_empty[NST] s_full[2] p_full[2] o_final[2] drain
   // ring_full[RING] ring_empty[RING]
-  static constexpr int NBAR = 2 + 3 * NST + 2 + 2 + 2 + 1 + 2 * RING;
+  static constexpr int NBAR = 2 + 2 * NST + 2 + 2 + 2 + 1 + 2 * RING;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;  // tmem base, abort flag, ring of unit ids
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16u + 4u * RING + 1024u;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -216,9 +217,8 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sQ[2] = {smem + C::OFF_Q, smem + C::OFF_Q + C::Q_BYTES};
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 2;
-  uint64_t* v_full = k_full + NST;
-  uint64_t* kv_empty = v_full + NST;
+  uint64_t* kv_full = bars + 2;
+  uint64_t* kv_empty = kv_full + NST;
   uint64_t* s_full = kv_empty + NST;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_final = p_full + 2;
@@ -235,19 +235,18 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&q_full[0], 1);
     mbar_init(&q_full[1], 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 2);  // one release per MMA thread
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);  // one elected arrival per softmax warp
       mbar_init(&o_final[i], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     for (int j = 0; j < C::RING; ++j) {
       mbar_init(&ring_full[j], 1);
-      mbar_init(&ring_empty[j], 1 + 8);  // MMA thread + one arrival per softmax warp
+      mbar_init(&ring_empty[j], 2 + 8);  // both MMA threads + one arrival per softmax warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -352,10 +351,9 @@ __global__ void __launch_bounds__(384, 1)
           const int row = u.bh * p.n + blk * BN;
           uint8_t* sk = smem + C::OFF_K + s * C::KV_BYTES;
           uint8_t* sv = smem + C::OFF_V + s * C::KV_BYTES;
-          mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
-          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sk + c * BN * ROWB, &tm_k, &k_full[s], c * C::CH, row);
-          mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
-          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sv + c * BN * ROWB, &tm_v, &v_full[s], c * C::CH, row);
+          mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
+          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sk + c * BN * ROWB, &tm_k, &kv_full[s], c * C::CH, row);
+          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sv + c * BN * ROWB, &tm_v, &kv_full[s], c * C::CH, row);
           ++k;
         }
         if (pc.c[0].bad || pc.c[1].bad) atomicOr(p.err, kErrBadSupport);
@@ -364,43 +362,42 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = (k > NST ? k - NST : 0); j < k; ++j) {
         const int s = j % NST;
         const uint32_t ph = (j / NST) & 1;
-        mbar_wait_drain(&k_full[s], ph, p.err);
-        mbar_wait_drain(&v_full[s], ph, p.err);
+        mbar_wait_drain(&kv_full[s], ph, p.err);
       }
       for (int i = 0; i < 2; ++i)
         if (nq[i] > 0) mbar_wait_drain(&q_full[i], (nq[i] - 1) & 1, p.err);
     }
     __syncwarp();
-   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+   } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per stream (warp 1: stream 0, warp 2: stream 1), so
+    // that one stream's waits overlap the other's MMA issue. Both walk the
+    // union of the unit's key blocks: a block the stream does not use is
+    // released at once, a used one after the stream's PV MMA on it.
     if (lane == 0) {
+      const int i = warp - 1;
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
       constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
       bool ok = true;
-      uint32_t nq[2] = {0u, 0u};    // units seen per stream (q_full / o_final phases)
-      uint32_t n_pt[2] = {0u, 0u};  // P tiles consumed per stream (p_full phases)
-      uint32_t n_pv[2] = {0u, 0u};  // PV MMAs in the current unit (accumulate flag)
-      bool pending[2] = {false, false};
-      int pend_slot[2] = {0, 0};
-      uint32_t pend_ph[2] = {0, 0};
-      uint32_t rem[NST];
-      for (int s = 0; s < NST; ++s) rem[s] = 0;
+      uint32_t nq = 0u;    // units using this stream (q_full / o_final phases)
+      uint32_t n_pt = 0u;  // P tiles consumed (p_full phases)
+      uint32_t n_pv = 0u;  // PV MMAs in the current unit (accumulate flag)
+      bool pending = false;
+      int pend_slot = 0;
 
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i], n_pt[i] & 1, abort_flag, p.err)) return false;
-        ++n_pt[i];
-        const int s = pend_slot[i];
-        if (!mbar_wait(&v_full[s], pend_ph[i], abort_flag, p.err)) return false;
+      auto flush_pv = [&]() -> bool {
+        if (!mbar_wait(&p_full[i], n_pt & 1, abort_flag, p.err)) return false;
+        ++n_pt;
         tc_fence_after();
-        const uint32_t vbase = smem_u32(smem + C::OFF_V + s * C::KV_BYTES);
+        const uint32_t vbase = smem_u32(smem + C::OFF_V + pend_slot * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bdesc = smem_desc(vbase + kk * 16 * ROWB, BN * ROWB, 8 * ROWB, C::SWZ);
-          umma_ts(tbase + C::o_col(i), tbase + C::s_col(i) + kk * 8, bdesc, IDESC_O, (n_pv[i] | kk) != 0);
+          umma_ts(tbase + C::o_col(i), tbase + C::s_col(i) + kk * 8, bdesc, IDESC_O, (n_pv | kk) != 0);
         }
-        ++n_pv[i];
-        if (--rem[s] == 0) umma_commit(&kv_empty[s]);
-        pending[i] = false;
+        ++n_pv;
+        umma_commit(&kv_empty[pend_slot]);
+        pending = false;
         return true;
       };
 
@@ -412,29 +409,26 @@ __global__ void __launch_bounds__(384, 1)
         if (id < 0) continue;
         Unit u;
         decode(id, u);
+        const bool active = (i == 0) || u.has1;
         PairCursor pc;
         make_cursor(pc.c[0], u, 0);
         make_cursor(pc.c[1], u, 1);
         pc.start();
-        bool q_ready[2] = {false, false};
-        n_pv[0] = n_pv[1] = 0;
+        bool q_ready = false;
+        n_pv = 0;
         int32_t blk;
         uint32_t who;
         while (ok && pc.next(blk, who)) {
           const int s = k % NST;
           const uint32_t ph = (k / NST) & 1;
-          bool k_ready = false;
-          rem[s] = __popc(who);
-          for (int i = 0; i < 2 && ok; ++i) {
-            if (pending[i] && !(ok = issue_pv(i))) break;
-            if (!(who & (1u << i))) continue;
-            if (!q_ready[i]) {
-              if (!(ok = mbar_wait(&q_full[i], nq[i] & 1, abort_flag, p.err))) break;
-              q_ready[i] = true;
-            }
-            if (!k_ready) {
-              if (!(ok = mbar_wait(&k_full[s], ph, abort_flag, p.err))) break;
-              k_ready = true;
+          if (pending && !(ok = flush_pv())) break;
+          // waiting for the block also keeps this thread from releasing a
+          // slot's next use before the other thread released this one
+          if (!(ok = mbar_wait(&kv_full[s], ph, abort_flag, p.err))) break;
+          if (who & (1u << i)) {
+            if (!q_ready) {
+              if (!(ok = mbar_wait(&q_full[i], nq & 1, abort_flag, p.err))) break;
+              q_ready = true;
             }
             tc_fence_after();
             const uint32_t qa = smem_u32(sQ[i]);
@@ -447,24 +441,24 @@ __global__ void __launch_bounds__(384, 1)
               umma_ss(tbase + C::s_col(i), adesc, bdesc, IDESC_S, kk > 0);
             }
             umma_commit(&s_full[i]);
-            pending[i] = true;
-            pend_slot[i] = s;
-            pend_ph[i] = ph;
+            pending = true;
+            pend_slot = s;
+          } else {
+            mbar_arrive(&kv_empty[s]);
           }
           ++k;
         }
-        for (int i = 0; i < 2 && ok; ++i)
-          if (pending[i]) ok = issue_pv(i);
-        // Close the unit for each stream it uses: its Q load has landed (so the
-        // next load into that buffer cannot overlap it) and o_final fires once
-        // every MMA issued so far has completed.
-        for (int i = 0; i < (u.has1 ? 2 : 1) && ok; ++i) {
-          if (!q_ready[i]) ok = mbar_wait(&q_full[i], nq[i] & 1, abort_flag, p.err);
+        if (ok && pending) ok = flush_pv();
+        // Close the unit for this stream: its Q load has landed (so the next
+        // load into the buffer cannot overlap it) and o_final fires once every
+        // MMA this thread issued has completed.
+        if (ok && active) {
+          if (!q_ready) ok = mbar_wait(&q_full[i], nq & 1, abort_flag, p.err);
           umma_commit(&o_final[i]);
-          ++nq[i];
+          ++nq;
         }
       }
-      umma_commit(drain);  // every MMA of this CTA done before TMEM is released
+      umma_commit(drain);  // every MMA of this thread done before TMEM is released
       mbar_wait_drain(drain, 0, p.err);
     }
     __syncwarp();

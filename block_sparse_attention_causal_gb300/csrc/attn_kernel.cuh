@@ -75,7 +75,8 @@ struct AttnCfg {
   // q_full[2] kv_full[NST] kv_empty[NST] s_full[2] p_full[2] o_final[2] drain
   // ring_full[RING] ring_empty[RING]
   static constexpr int NBAR = 2 + 2 * NST + 2 + 2 + 2 + 1 + 2 * RING;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;  // tmem base, abort flag, ring of unit ids
+  // tmem base (+0), abort flag (+4), softmax lock (+8), ring of unit ids (+16)
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16u + 4u * RING + 1024u;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns: S/P of stream i at s_col(i), O of stream i at o_col(i)
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(384, 1)
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  int* sm_lock = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -244,6 +246,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&o_final[i], 1);
     }
     mbar_init(drain, 2);
+    *sm_lock = 0;
     for (int j = 0; j < C::RING; ++j) {
       mbar_init(&ring_full[j], 1);
       mbar_init(&ring_empty[j], 2 + 8);  // both MMA threads + one arrival per softmax warp
@@ -508,6 +511,19 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         ++n_s;
         tc_fence_after();
+        // Dense steps: only one softmax warpgroup computes at a time, so the
+        // other stream's MMAs run while this one works (ping-pong) and the two
+        // never split the SM's issue slots. (Sparse steps, whose two streams
+        // often have different blocks, run faster without the lock.)
+        if (!SPARSE) {
+          if (r == 0) {
+            for (;;) {
+              if (*reinterpret_cast<volatile int*>(sm_lock) == 0 && atomicCAS(sm_lock, 0, 1) == 0) break;
+              __nanosleep(20);
+            }
+          }
+          named_bar_sync(3 + i, 128);
+        }
         const int kbase = blk * BN;
         const bool row_on = (mask >> half) & 1u;
         // columns c <= limit are admissible (causal mask M, working-set mask R)
@@ -545,9 +561,9 @@ __global__ void __launch_bounds__(384, 1)
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         // P = 2^(s*scale*log2e - m) as bf16 pairs, written over S. Packed f32x2
-        // FMA for the exponent argument and packed adds (two independent
-        // accumulators each) for the fp32 and bf16 row sums. Masked entries
-        // hold -inf and give exactly 0.
+        // FMA for the exponent argument, a packed add for the fp32 row sum and
+        // mixed bf16+f32 adds for the sum of the rounded P (two independent
+        // accumulators each). Masked entries hold -inf and give exactly 0.
         const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
         uint64_t rs2[2] = {0ull, 0ull}, rt2[2] = {0ull, 0ull};
 #pragma unroll
@@ -562,7 +578,7 @@ __global__ void __launch_bounds__(384, 1)
             const float p1 = fast_exp2(e1);
             pk[j] = pack_bf16x2(p0, p1);
             rs2[j & 1] = fadd2(rs2[j & 1], f2_pack(p0, p1));
-            rt2[j & 1] = fadd2(rt2[j & 1], f2_pack(__uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xFFFF0000u)));
+            add_bf16x2_to(rt2[j & 1], pk[j]);
           }
           tmem_st_x16(tS + cc * 16, pk);
         }
@@ -588,6 +604,10 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         tmem_wait_st();
+        if (!SPARSE) {
+          named_bar_sync(3 + i, 128);
+          if (r == 0) atomicExch(sm_lock, 0);
+        }
         if (want_mass) lam[(size_t)cnt * 128] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
         tc_fence_before();
         __syncwarp();

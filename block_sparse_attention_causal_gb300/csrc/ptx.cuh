@@ -230,6 +230,16 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// acc (an f32 pair) += the two bf16 halves of `packed`, each widened exactly.
+__device__ __forceinline__ void add_bf16x2_to(uint64_t& acc, uint32_t packed) {
+  unsigned short lo, hi;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(packed));
+  float a, b;
+  f2_unpack(acc, a, b);
+  asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(a) : "h"(lo));
+  asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(b) : "h"(hi));
+  acc = f2_pack(a, b);
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

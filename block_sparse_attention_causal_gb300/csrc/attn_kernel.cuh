@@ -7,25 +7,26 @@
 //  * reuse    (SPARSE = true): attention restricted to the CSR block support,
 //    §5.2 Eqs 7-8 -- only listed key blocks are loaded and multiplied.
 //
-// Persistent: one CTA per SM pulls work units (two 128-row query tiles,
-// "streams", of one (batch, head)) from the work order, heaviest first. While one unit's epilogue
-// runs, the next unit's Q/K/V loads and first MMAs proceed. Warp roles (384
-// threads, three warpgroups):
-//   warp 0      TMA producer: Q tiles once, then K/V blocks into an NST ring
-//   warp 1      TMEM allocator + MMA issuer of stream 0 (single thread)
-//   warp 2      MMA issuer of stream 1 (single thread)
-//   warp 3      idle (the control warpgroup gives its registers away)
-//   warps 4-7   softmax warpgroup of stream 0 (one query row per thread)
-//   warps 8-11  softmax warpgroup of stream 1
-// Registers are moved from the control warpgroup (96 each) to the softmax
-// warpgroups (200 each): 128*96 + 256*200 <= 384*168, the launch allocation.
-// Both MMA threads walk the ascending union of the two streams' key-block
-// lists; a K/V block read by both streams is loaded once. Per stream, S = Q K^T goes
-// to its own TMEM columns; the softmax warps turn S into P (bf16, written
-// back over S) and the MMA thread accumulates O += P V from TMEM. While one
-// stream's warps run the softmax, the tensor core works on the other stream.
-// The running row max is only moved (and O rescaled) when it grows by more
-// than 2^8, so most tiles skip the O correction.
+// Persistent: one CTA per SM pulls work units (one 128-row query tile of one
+// (batch, head)) from the work order, heaviest first. The key blocks of all
+// units a CTA takes form one continuous stream of "entries"; the pipeline runs
+// across unit boundaries. Warp roles (512 threads, four warpgroups):
+//   warp 0      scheduler: claims units, walks their key-block lists, and
+//               publishes one record per entry in a shared-memory ring
+//   warp 1      TMA loads of Q (once per unit), K (ring of NK slots) and V
+//               (ring of NV slots)
+//   warp 2      issues the S = Q K^T MMAs (one elected lane)
+//   warp 3      TMEM allocator; issues the O += P V MMAs (one elected lane)
+//   warps 4-7   softmax warpgroup 0: key columns [0, BN/2) of every row
+//   warps 8-11  softmax warpgroup 1: key columns [BN/2, BN)
+//   warps 12-15 epilogue: O normalisation and store, LSE, block masses
+// TMEM holds three S buffers and the O accumulator. S for entry j+1 and j+2
+// is computed while the softmax works on entry j; P (bf16) is written over
+// S_j and consumed from TMEM by the PV MMA, after which S_{j+3} reuses the
+// buffer. The two softmax warpgroups split each score row and exchange row
+// maxima through shared memory. The running row max is only moved (and O
+// rescaled) when it grows by more than 2^8, so most entries skip the O
+// correction.
 #pragma once
 #include <stdint.h>
 
@@ -44,6 +45,16 @@ struct SchedSlot {
 constexpr int kSchedSlots = 256;
 static __device__ SchedSlot g_sched[kSchedSlots];
 
+// Flags of an entry record.
+enum : uint32_t {
+  kEntFirst = 1u,   // first entry of its unit
+  kEntLast = 2u,    // last entry of its unit
+  kEntEnd = 4u,     // no more entries: the CTA's work is done
+  kEntQbuf = 8u,    // Q buffer of the unit
+  kEntRows0 = 16u,  // the rows of query block 0 of the tile list this key block
+  kEntRows1 = 32u,  // ... of query block 1 (BN = 64 only)
+};
+
 template <int D, int BN, bool SPARSE>
 struct AttnCfg {
   static_assert(D == 64 || D == 96 || D == 128, "head_dim");
@@ -54,35 +65,45 @@ struct AttnCfg {
   static constexpr uint32_t ROWB = CH * 2;               // bytes per swizzled row
   static constexpr uint32_t Q_BYTES = 128u * D * 2u;
   static constexpr uint32_t KV_BYTES = (uint32_t)BN * D * 2u;
-  static constexpr uint32_t SMEM_BUDGET = 230400u;
+  static constexpr int THREADS = 512;
+  static constexpr int NSB = 3;       // S buffers in TMEM
+  static constexpr int META = 32;     // entry records in flight
+  static constexpr int URING = 8;     // unit records in flight (epilogue)
+  static constexpr int HB = BN / 2;   // key columns per softmax warpgroup
   static constexpr int MAX_NB = 1024;
-  // per-warp partial block masses of the Eq 5 epilogue, [2 streams][4 warps][nb]
-  static constexpr uint32_t PART_BYTES = SPARSE ? 0u : 2u * 4u * MAX_NB * 4u;
-  static constexpr int NST_FIT = (int)((SMEM_BUDGET - 2u * Q_BYTES - PART_BYTES) / (2u * KV_BYTES));
-  static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;  // K/V ring depth
-  static_assert(NST >= 2, "ring");
-  static constexpr int THREADS = 384;
-  static constexpr uint32_t REGS_CONTROL = 104, REGS_SOFTMAX = 200, REGS_LAUNCH = 168;
-  // setmaxnreg.inc waits for registers released by setmaxnreg.dec: the split
-  // must fit in what the CTA was launched with (checked against ptxas -v).
-  static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= THREADS * REGS_LAUNCH, "register split");
+  static constexpr int ENT_PER_TILE = 128 / BN;  // query blocks per 128-row tile
+  // shared memory: Q[2] | K[NK] | V[NV] | xch | stats | part | meta | units | barriers | misc
+  static constexpr uint32_t XCH_BYTES = 2u * 2u * 128u * 4u;    // row-max exchange, two tiles
+  static constexpr uint32_t STATS_BYTES = 2u * 5u * 128u * 4u;  // per-row m, l, lt of two units
+  static constexpr uint32_t PART_BYTES = SPARSE ? 0u : 4u * 64u * 4u;
+  static constexpr uint32_t META_BYTES = META * 16u;
+  static constexpr uint32_t URING_BYTES = URING * 8u;
+  static constexpr int NBAR_FIXED = 2 + 2 + 3 * NSB + 2 + 2 + 2 + 2 * URING + 2;
+  static constexpr uint32_t SMEM_LIMIT = 232448u;  // 227 KB per CTA
+  static constexpr uint32_t FIXED = 2u * Q_BYTES + XCH_BYTES + STATS_BYTES + PART_BYTES + META_BYTES + URING_BYTES +
+                                    (NBAR_FIXED + 16) * 8u + 32u + 1024u;
+  static constexpr int SLOTS_FIT = (int)((SMEM_LIMIT - FIXED) / KV_BYTES);
+  static constexpr int NK = SLOTS_FIT >= 8 ? 4 : (SLOTS_FIT + 1) / 2;
+  static constexpr int NV = SLOTS_FIT >= 8 ? 4 : SLOTS_FIT / 2;
+  static_assert(NK >= 2 && NV >= 2, "K/V rings");
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2u * Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
-  static constexpr uint32_t OFF_PART = OFF_V + NST * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_PART + PART_BYTES;
-  static constexpr int RING = 4;  // work units published to the consumer roles
-  // q_full[2] kv_full[NST] kv_empty[NST] s_full[2] p_full[2] o_final[2] drain
-  // ring_full[RING] ring_empty[RING]
-  static constexpr int NBAR = 2 + 2 * NST + 2 + 2 + 2 + 1 + 2 * RING;
-  // tmem base (+0), abort flag (+4), softmax lock (+8), ring of unit ids (+16)
+  static constexpr uint32_t OFF_V = OFF_K + NK * KV_BYTES;
+  static constexpr uint32_t OFF_XCH = OFF_V + NV * KV_BYTES;
+  static constexpr uint32_t OFF_STATS = OFF_XCH + XCH_BYTES;
+  static constexpr uint32_t OFF_PART = OFF_STATS + STATS_BYTES;
+  static constexpr uint32_t OFF_META = OFF_PART + PART_BYTES;
+  static constexpr uint32_t OFF_URING = OFF_META + META_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_URING + URING_BYTES;
+  static constexpr int NBAR = NBAR_FIXED + 2 * NK + 2 * NV;
+  // tmem base (+0), abort flag (+4), entries whose PV was issued (+8),
+  // softmax abort entry (+12), epilogue abort unit (+16)
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16u + 4u * RING + 1024u;  // + alignment slack
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32u + 1024u;  // + alignment slack
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM columns: S/P of stream i at s_col(i), O of stream i at o_col(i)
-  __host__ __device__ static constexpr uint32_t s_col(int i) { return i ? 128u : 0u; }
-  __host__ __device__ static constexpr uint32_t o_col(int i) { return i ? 384u : 256u; }
-  static constexpr int ENT_PER_TILE = 128 / BN;  // key blocks per 128 rows
+  __host__ __device__ static constexpr uint32_t s_col(int b) { return 128u * (uint32_t)b; }
+  static constexpr uint32_t O_COL = 384;
 };
 
 // Entries (key blocks) of one 128-row query tile in ascending order. Dense:
@@ -110,12 +131,6 @@ struct TileCursor {
     return INT32_MAX;
   }
 
-  __device__ __forceinline__ void init_empty() {
-    sparse = false;
-    next_dense = 0;
-    dense_end = 0;
-    bad = false;
-  }
   __device__ __forceinline__ void init_dense(int t, const AttnParams& p, int bn) {
     sparse = false;
     bad = false;
@@ -163,42 +178,23 @@ struct TileCursor {
   }
 };
 
-// Ascending union of the two streams' entries; `who` bit i = stream i uses it.
-struct PairCursor {
-  TileCursor c[2];
-  int32_t head[2];
-  __device__ __forceinline__ void start() {
-    uint32_t m;
-    for (int i = 0; i < 2; ++i)
-      if (!c[i].next(head[i], m)) head[i] = INT32_MAX;
-  }
-  __device__ __forceinline__ bool next(int32_t& blk, uint32_t& who) {
-    if (head[0] == INT32_MAX && head[1] == INT32_MAX) return false;
-    blk = min(head[0], head[1]);
-    who = (head[0] == blk ? 1u : 0u) | (head[1] == blk ? 2u : 0u);
-    uint32_t m;
-    for (int i = 0; i < 2; ++i)
-      if (head[i] == blk && !c[i].next(head[i], m)) head[i] = INT32_MAX;
-    return true;
-  }
-};
-
 // Default order of work units: (batch, head) slices in groups sized so the
 // group's K/V stays in L2, heavier (later) query tiles first inside a group.
 __device__ __forceinline__ int64_t default_unit(int64_t x, const AttnParams& p) {
   const int64_t g_heads = p.group_heads;
-  const int64_t per_group = g_heads * p.npairs;
+  const int64_t per_group = g_heads * p.n_qtiles;
   const int64_t g = x / per_group, w = x % per_group;
   const int64_t gsize = min(g_heads, (int64_t)p.bh_count - g * g_heads);
-  const int64_t pr = p.npairs - 1 - w / gsize;
+  const int64_t t = p.n_qtiles - 1 - w / gsize;
   const int64_t bh = g * g_heads + w % gsize;
-  return bh * p.npairs + pr;
+  return bh * p.n_qtiles + t;
 }
 
+// First float of tile t's Eq 5 scratch: per entry, two halves of 128 rows.
 __device__ __forceinline__ int64_t lam_tile_offset(int bh, int t, const AttnParams& p, int ept) {
   const int64_t before = (int64_t)ept * t * (t + 1) / 2;
   const int64_t total = (int64_t)ept * p.n_qtiles * (p.n_qtiles + 1) / 2;
-  return ((int64_t)bh * total + before) * 128;
+  return ((int64_t)bh * total + before) * 256;
 }
 
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* err) {
@@ -206,55 +202,144 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return mbar_wait(bar, parity, &dummy_abort, err);
 }
 
+// Entry records: word 0 is the tag (entry index + 1), written last.
+struct EntryRec {
+  uint32_t tag;
+  uint32_t krow;   // global row of the key block's first key (TMA coordinate)
+  uint32_t unit;   // unit id = bh * n_qtiles + tile
+  uint32_t info;   // flags | block index << 8
+};
+
+// Wait until record j is published; false on abort/timeout or if the ring
+// was overrun (which the scheduler's flow control rules out). The spin is out
+// of line; the common case (already published) is one load and a compare.
+static __device__ __noinline__ bool wait_entry_slow(EntryRec* r, uint32_t j, volatile int* abort_flag, uint32_t* err) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    const uint32_t tag = ld_acquire_smem(&r->tag);
+    if (tag == j + 1u) return true;
+    if (tag > j + 1u) {
+      *abort_flag = 1;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool wait_entry(EntryRec* ring, int meta, uint32_t j, EntryRec& out,
+                                           volatile int* abort_flag, uint32_t* err) {
+  EntryRec* r = ring + (j % (uint32_t)meta);
+  if (ld_acquire_smem(&r->tag) != j + 1u && !wait_entry_slow(r, j, abort_flag, err)) return false;
+  out.tag = j + 1u;
+  out.krow = r->krow;
+  out.unit = r->unit;
+  out.info = r->info;
+  return true;
+}
+
+// O row segment [tO, tO + ncols) *= factor (the lazy rescale, rare).
+static __device__ __noinline__ void rescale_o(uint32_t tO, int ncols, float factor) {
+  for (int c = 0; c < ncols; c += 8) {
+    uint32_t o[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]), "=r"(o[4]), "=r"(o[5]), "=r"(o[6]), "=r"(o[7])
+                 : "r"(tO + c)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(o[0]), "+r"(o[1]), "+r"(o[2]), "+r"(o[3]), "+r"(o[4]), "+r"(o[5]), "+r"(o[6]), "+r"(o[7])
+                 :
+                 : "memory");
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * factor);
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tO + c), "r"(o[0]),
+                 "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                 : "memory");
+  }
+}
+
 template <int D, int BN, bool SPARSE>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     wise_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   using C = AttnCfg<D, BN, SPARSE>;
-  constexpr int NST = C::NST;
+  constexpr int NK = C::NK, NV = C::NV, NSB = C::NSB, META = C::META, URING = C::URING;
   constexpr uint32_t ROWB = C::ROWB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ[2] = {smem + C::OFF_Q, smem + C::OFF_Q + C::Q_BYTES};
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 2;
-  uint64_t* kv_empty = kv_full + NST;
-  uint64_t* s_full = kv_empty + NST;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_final = p_full + 2;
-  uint64_t* drain = o_final + 2;
-  uint64_t* ring_full = drain + 1;
-  uint64_t* ring_empty = ring_full + C::RING;
-  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  volatile int* ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
-  int* sm_lock = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+  uint64_t* q_full = bars;              // [2]
+  uint64_t* q_empty = q_full + 2;       // [2]
+  uint64_t* s_full = q_empty + 2;       // [NSB]
+  uint64_t* p_full = s_full + NSB;      // [NSB]
+  uint64_t* pv_done = p_full + NSB;     // [NSB]
+  uint64_t* o_final = pv_done + NSB;    // [1]
+  uint64_t* o_free = o_final + 1;       // [1]
+  uint64_t* st_full = o_free + 1;       // [2]
+  uint64_t* st_empty = st_full + 2;     // [2]
+  uint64_t* u_full = st_empty + 2;      // [URING]
+  uint64_t* u_empty = u_full + URING;   // [URING]
+  uint64_t* drain = u_empty + URING;    // [2]
+  uint64_t* k_full = drain + 2;         // [NK]
+  uint64_t* k_empty = k_full + NK;      // [NK]
+  uint64_t* v_full = k_empty + NK;      // [NV]
+  uint64_t* v_empty = v_full + NV;      // [NV]
+  EntryRec* meta = reinterpret_cast<EntryRec*>(smem + C::OFF_META);
+  int32_t* uring = reinterpret_cast<int32_t*>(smem + C::OFF_URING);  // {unit id, entries}
+  float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+  float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS);
+  float* part = reinterpret_cast<float*>(smem + C::OFF_PART);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  uint32_t* tmem_base_slot = misc;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  uint32_t* pv_issued = misc + 2;
+  int* sm_abort = reinterpret_cast<int*>(misc + 3);
+  int* ep_abort = reinterpret_cast<int*>(misc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&q_full[0], 1);
-    mbar_init(&q_full[1], 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 2);  // one release per MMA thread
-    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);  // one elected arrival per softmax warp
-      mbar_init(&o_final[i], 1);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&st_full[i], 8);   // one arrival per softmax warp
+      mbar_init(&st_empty[i], 4);  // one arrival per epilogue warp
     }
-    mbar_init(drain, 2);
-    *sm_lock = 0;
-    for (int j = 0; j < C::RING; ++j) {
-      mbar_init(&ring_full[j], 1);
-      mbar_init(&ring_empty[j], 2 + 8);  // both MMA threads + one arrival per softmax warp
+    for (int b = 0; b < NSB; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 8);
+      mbar_init(&pv_done[b], 1);
     }
+    mbar_init(o_final, 1);
+    mbar_init(o_free, 4);
+    for (int j = 0; j < URING; ++j) {
+      mbar_init(&u_full[j], 1);
+      mbar_init(&u_empty[j], 4);
+    }
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int j = 0; j < META; ++j) meta[j].tag = 0u;
     *abort_flag = 0;
+    *pv_issued = 0u;
+    *sm_abort = INT32_MAX;
+    *ep_abort = INT32_MAX;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 3) {
     tmem_alloc(tmem_base_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -263,439 +348,537 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_base_slot;
 
-  // Work distribution: the producer thread pulls positions x of the work
-  // order from the launch's counter (greedy, heaviest units first) and
-  // publishes the unit ids through a shared-memory ring; every other role
-  // reads the same sequence from the ring. -1 ends the sequence, -2 marks a
-  // malformed schedule entry (skipped).
-  struct Unit {
-    int bh, tile[2];
-    bool has1;
-  };
-  auto decode = [&](int id, Unit& u) {
-    u.bh = id / p.npairs;
-    const int pair = id % p.npairs;
-    u.tile[0] = 2 * pair;
-    u.tile[1] = 2 * pair + 1;
-    u.has1 = u.tile[1] < p.n_qtiles;
-  };
-  // consumer side: next unit id from the ring (-1 at the end or on abort)
-  auto ring_take = [&](int& ci, bool warp_vote) -> int {
-    const int slot = ci % C::RING;
-    bool okw = mbar_wait(&ring_full[slot], (ci / C::RING) & 1, abort_flag, p.err);
-    if (warp_vote) okw = __all_sync(0xffffffffu, okw);
-    if (!okw) return -1;
-    const int id = ring[slot];
-    if (warp_vote) {
-      __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(&ring_empty[slot]);
-    } else {
-      mbar_arrive(&ring_empty[slot]);
-    }
-    ++ci;
-    return id;
-  };
-  auto make_cursor = [&](TileCursor& c, const Unit& u, int i) {
-    if (i == 1 && !u.has1) {
-      c.init_empty();
-    } else if (SPARSE) {
-      c.init_sparse(u.tile[i], u.bh, p, C::ENT_PER_TILE);
-    } else {
-      c.init_dense(u.tile[i], p, BN);
-    }
-  };
-
-  if (warp < 4) {
-   setmaxnreg_dec<C::REGS_CONTROL>();
-   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0) {
+    // ------------------------------------------------------------ scheduler
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      uint32_t nq[2] = {0u, 0u};  // Q loads per stream (one per unit using it)
-      int k = 0;                  // K/V loads issued (ring position)
-      bool ok = true;
       SchedSlot* sched = &g_sched[p.sched_slot];
-      for (int pi = 0; ok; ++pi) {
-        const int slot = pi % C::RING;
-        if (pi >= C::RING && !(ok = mbar_wait(&ring_empty[slot], ((pi / C::RING) - 1) & 1, abort_flag, p.err)))
-          break;
+      uint32_t j = 0;  // entries published
+      int u = 0;       // units published
+      int uq = 0;      // units with at least one entry
+      bool ok = true;
+      // publish one entry record, after the flow control allows slot j
+      auto publish = [&](uint32_t krow, uint32_t unit, uint32_t info) -> bool {
+        if (j >= (uint32_t)META) {
+          const uint64_t t0 = global_timer_ns();
+          for (uint32_t it = 0; j >= ld_acquire_smem(pv_issued) + (uint32_t)META; ++it) {
+            if ((it & 63u) == 63u) {
+              if (*abort_flag) return false;
+              if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(p.err, kErrTimeout);
+                return false;
+              }
+            }
+            __nanosleep(64);
+          }
+        }
+        EntryRec* r = meta + (j % (uint32_t)META);
+        r->krow = krow;
+        r->unit = unit;
+        r->info = info;
+        st_release_smem(&r->tag, j + 1u);
+        ++j;
+        return true;
+      };
+      while (ok) {
         const unsigned int x = atomicAdd(&sched->next, 1u);
         int id = -1;
         if ((int64_t)x < p.n_units) {
           const int64_t v = (SPARSE && p.tile_order != nullptr) ? (int64_t)__ldg(p.tile_order + x) : default_unit(x, p);
           id = (v >= 0 && v < p.n_units) ? (int)v : -2;
-          if (id == -2) atomicOr(p.err, kErrBadSupport);
-        }
-        ring[slot] = id;
-        mbar_arrive(&ring_full[slot]);
-        if (id == -1) break;
-        if (id < 0) continue;
-        Unit u;
-        decode(id, u);
-        for (int i = 0; i < (u.has1 ? 2 : 1) && ok; ++i) {
-          // the previous unit that used Q_i has finished all its MMAs
-          if (nq[i] > 0 && !(ok = mbar_wait(&o_final[i], (nq[i] - 1) & 1, abort_flag, p.err))) break;
-          const int row = u.bh * p.n + u.tile[i] * 128;
-          mbar_arrive_expect_tx(&q_full[i], C::Q_BYTES);
-          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sQ[i] + c * 128 * ROWB, &tm_q, &q_full[i], c * C::CH, row);
-          ++nq[i];
-        }
-        PairCursor pc;
-        make_cursor(pc.c[0], u, 0);
-        make_cursor(pc.c[1], u, 1);
-        pc.start();
-        int32_t blk;
-        uint32_t who;
-        while (ok && pc.next(blk, who)) {
-          const int s = k % NST;
-          if (k >= NST && !(ok = mbar_wait(&kv_empty[s], ((k / NST) - 1) & 1, abort_flag, p.err))) break;
-          const int row = u.bh * p.n + blk * BN;
-          uint8_t* sk = smem + C::OFF_K + s * C::KV_BYTES;
-          uint8_t* sv = smem + C::OFF_V + s * C::KV_BYTES;
-          mbar_arrive_expect_tx(&kv_full[s], 2 * C::KV_BYTES);
-          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sk + c * BN * ROWB, &tm_k, &kv_full[s], c * C::CH, row);
-          for (int c = 0; c < C::NCH; ++c) tma_load_2d(sv + c * BN * ROWB, &tm_v, &kv_full[s], c * C::CH, row);
-          ++k;
-        }
-        if (pc.c[0].bad || pc.c[1].bad) atomicOr(p.err, kErrBadSupport);
-      }
-      // No copy into this CTA's shared memory may outlive the CTA.
-      for (int j = (k > NST ? k - NST : 0); j < k; ++j) {
-        const int s = j % NST;
-        const uint32_t ph = (j / NST) & 1;
-        mbar_wait_drain(&kv_full[s], ph, p.err);
-      }
-      for (int i = 0; i < 2; ++i)
-        if (nq[i] > 0) mbar_wait_drain(&q_full[i], (nq[i] - 1) & 1, p.err);
-    }
-    __syncwarp();
-   } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers
-    // One issuing thread per stream (warp 1: stream 0, warp 2: stream 1), so
-    // that one stream's waits overlap the other's MMA issue. Both walk the
-    // union of the unit's key blocks: a block the stream does not use is
-    // released at once, a used one after the stream's PV MMA on it.
-    if (lane == 0) {
-      const int i = warp - 1;
-      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
-      constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
-      bool ok = true;
-      uint32_t nq = 0u;    // units using this stream (q_full / o_final phases)
-      uint32_t n_pt = 0u;  // P tiles consumed (p_full phases)
-      uint32_t n_pv = 0u;  // PV MMAs in the current unit (accumulate flag)
-      bool pending = false;
-      int pend_slot = 0;
-
-      auto flush_pv = [&]() -> bool {
-        if (!mbar_wait(&p_full[i], n_pt & 1, abort_flag, p.err)) return false;
-        ++n_pt;
-        tc_fence_after();
-        const uint32_t vbase = smem_u32(smem + C::OFF_V + pend_slot * C::KV_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bdesc = smem_desc(vbase + kk * 16 * ROWB, BN * ROWB, 8 * ROWB, C::SWZ);
-          umma_ts(tbase + C::o_col(i), tbase + C::s_col(i) + kk * 8, bdesc, IDESC_O, (n_pv | kk) != 0);
-        }
-        ++n_pv;
-        umma_commit(&kv_empty[pend_slot]);
-        pending = false;
-        return true;
-      };
-
-      int k = 0;
-      int ci = 0;
-      while (ok) {
-        const int id = ring_take(ci, false);
-        if (id == -1) break;
-        if (id < 0) continue;
-        Unit u;
-        decode(id, u);
-        const bool active = (i == 0) || u.has1;
-        PairCursor pc;
-        make_cursor(pc.c[0], u, 0);
-        make_cursor(pc.c[1], u, 1);
-        pc.start();
-        bool q_ready = false;
-        n_pv = 0;
-        int32_t blk;
-        uint32_t who;
-        while (ok && pc.next(blk, who)) {
-          const int s = k % NST;
-          const uint32_t ph = (k / NST) & 1;
-          if (pending && !(ok = flush_pv())) break;
-          // waiting for the block also keeps this thread from releasing a
-          // slot's next use before the other thread released this one
-          if (!(ok = mbar_wait(&kv_full[s], ph, abort_flag, p.err))) break;
-          if (who & (1u << i)) {
-            if (!q_ready) {
-              if (!(ok = mbar_wait(&q_full[i], nq & 1, abort_flag, p.err))) break;
-              q_ready = true;
-            }
-            tc_fence_after();
-            const uint32_t qa = smem_u32(sQ[i]);
-            const uint32_t ka = smem_u32(smem + C::OFF_K + s * C::KV_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const int c = kk / (C::CH / 16), w = kk % (C::CH / 16);
-              const uint64_t adesc = smem_desc(qa + c * 128 * ROWB + w * 32, 16, 8 * ROWB, C::SWZ);
-              const uint64_t bdesc = smem_desc(ka + c * BN * ROWB + w * 32, 16, 8 * ROWB, C::SWZ);
-              umma_ss(tbase + C::s_col(i), adesc, bdesc, IDESC_S, kk > 0);
-            }
-            umma_commit(&s_full[i]);
-            pending = true;
-            pend_slot = s;
-          } else {
-            mbar_arrive(&kv_empty[s]);
+          if (id == -2) {
+            atomicOr(p.err, kErrBadSupport);
+            continue;
           }
-          ++k;
         }
-        if (ok && pending) ok = flush_pv();
-        // Close the unit for this stream: its Q load has landed (so the next
-        // load into the buffer cannot overlap it) and o_final fires once every
-        // MMA this thread issued has completed.
-        if (ok && active) {
-          if (!q_ready) ok = mbar_wait(&q_full[i], nq & 1, abort_flag, p.err);
-          umma_commit(&o_final[i]);
-          ++nq;
+        if (id == -1) break;
+        const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
+        TileCursor cur;
+        if (SPARSE) cur.init_sparse(t, bh, p, C::ENT_PER_TILE);
+        else cur.init_dense(t, p, BN);
+        const uint32_t qbuf = (uq & 1) ? kEntQbuf : 0u;
+        int cnt = 0;
+        int32_t blk, pblk = -1;
+        uint32_t mask, pmask = 0;
+        while (cur.next(blk, mask)) {
+          if (cnt > 0) {
+            const uint32_t info = (cnt == 1 ? kEntFirst : 0u) | qbuf | (pmask << 4) | ((uint32_t)pblk << 8);
+            if (!(ok = publish((uint32_t)(bh * p.n + pblk * BN), (uint32_t)id, info))) break;
+          }
+          pblk = blk;
+          pmask = mask;
+          ++cnt;
+        }
+        if (!ok) break;
+        if (cnt > 0) {
+          const uint32_t info = (cnt == 1 ? kEntFirst : 0u) | kEntLast | qbuf | (pmask << 4) | ((uint32_t)pblk << 8);
+          if (!(ok = publish((uint32_t)(bh * p.n + pblk * BN), (uint32_t)id, info))) break;
+          ++uq;
+        }
+        if (cur.bad) atomicOr(p.err, kErrBadSupport);
+        const int slot = u % URING;
+        if (u >= URING && !(ok = mbar_wait(&u_empty[slot], ((u / URING) - 1) & 1, abort_flag, p.err))) break;
+        uring[2 * slot] = id;
+        uring[2 * slot + 1] = cnt;
+        mbar_arrive(&u_full[slot]);
+        ++u;
+      }
+      if (ok) ok = publish(0u, 0u, kEntEnd);
+      if (ok) {
+        const int slot = u % URING;
+        if (u < URING || mbar_wait(&u_empty[slot], ((u / URING) - 1) & 1, abort_flag, p.err)) {
+          uring[2 * slot] = -1;
+          uring[2 * slot + 1] = 0;
+          mbar_arrive(&u_full[slot]);
         }
       }
-      umma_commit(drain);  // every MMA of this thread done before TMEM is released
-      mbar_wait_drain(drain, 0, p.err);
     }
     __syncwarp();
-   }
-  } else {
-    setmaxnreg_inc<C::REGS_SOFTMAX>();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ TMA loads
+    // Q (at the first entry of each unit), K and V. K runs KLEAD entries ahead
+    // of V: entry j's K is needed for S_j, which precedes the softmax and PV_j,
+    // which need V_j. The whole warp runs the loop; one elected lane issues.
+    const bool leader = elect_one();
+    constexpr int KLEAD = (NK - 1 < 2) ? NK - 1 : 2;
+    if (leader) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    uint32_t nq[2] = {0u, 0u};  // Q loads per buffer
+    uint32_t jk = 0, jv = 0;    // K and V loads issued
+    bool k_end = false, ok = true;
+    while (ok) {
+      // K for entry jk while it is at most KLEAD ahead of V
+      while (ok && !k_end && jk <= jv + KLEAD) {
+        EntryRec e;
+        ok = __all_sync(0xffffffffu, wait_entry(meta, META, jk, e, abort_flag, p.err));
+        if (!ok) break;
+        if (e.info & kEntEnd) {
+          k_end = true;
+          break;
+        }
+        if (e.info & kEntFirst) {
+          const int qb = (e.info & kEntQbuf) ? 1 : 0;
+          // the previous unit in this buffer has finished its S MMAs
+          if (nq[qb] > 0) ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[qb], (nq[qb] - 1) & 1, abort_flag, p.err));
+          if (!ok) break;
+          const int bh = (int)e.unit / p.n_qtiles, t = (int)e.unit % p.n_qtiles;
+          const int row = bh * p.n + t * 128;
+          uint8_t* sq = smem + C::OFF_Q + qb * C::Q_BYTES;
+          if (leader) {
+            mbar_arrive_expect_tx(&q_full[qb], C::Q_BYTES);
+            for (int c = 0; c < C::NCH; ++c) tma_load_2d(sq + c * 128 * ROWB, &tm_q, &q_full[qb], c * C::CH, row);
+          }
+          ++nq[qb];
+        }
+        const int s = (int)(jk % NK);
+        if (jk >= (uint32_t)NK) ok = __all_sync(0xffffffffu, mbar_wait(&k_empty[s], ((jk / NK) - 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        uint8_t* dst = smem + C::OFF_K + s * C::KV_BYTES;
+        if (leader) {
+          mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
+          for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * BN * ROWB, &tm_k, &k_full[s], c * C::CH, (int)e.krow);
+        }
+        ++jk;
+        __syncwarp();
+      }
+      if (!ok || jv == jk) break;  // jv == jk only once the entry stream has ended
+      // V for entry jv (its record is already published)
+      EntryRec e;
+      ok = __all_sync(0xffffffffu, wait_entry(meta, META, jv, e, abort_flag, p.err));
+      if (!ok) break;
+      const int s = (int)(jv % NV);
+      if (jv >= (uint32_t)NV) ok = __all_sync(0xffffffffu, mbar_wait(&v_empty[s], ((jv / NV) - 1) & 1, abort_flag, p.err));
+      if (!ok) break;
+      uint8_t* dst = smem + C::OFF_V + s * C::KV_BYTES;
+      if (leader) {
+        mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
+        for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * BN * ROWB, &tm_v, &v_full[s], c * C::CH, (int)e.krow);
+      }
+      ++jv;
+      __syncwarp();
+    }
+    // No copy into this CTA's shared memory may outlive the CTA.
+    if (leader) {
+      for (uint32_t i = (jk > (uint32_t)NK ? jk - NK : 0u); i < jk; ++i)
+        mbar_wait_drain(&k_full[i % NK], (i / NK) & 1, p.err);
+      for (uint32_t i = (jv > (uint32_t)NV ? jv - NV : 0u); i < jv; ++i)
+        mbar_wait_drain(&v_full[i % NV], (i / NV) & 1, p.err);
+      for (int qb = 0; qb < 2; ++qb)
+        if (nq[qb] > 0) mbar_wait_drain(&q_full[qb], (nq[qb] - 1) & 1, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 2 issues S_j = Q K_j^T, warp 3 issues O += P_j V_j. Each whole warp
+    // runs its loop (barrier waits and descriptor arithmetic stay warp-uniform)
+    // and one elected lane issues the MMAs and their commits: single-lane
+    // issue loops lose most of their issue slots to the softmax warps sharing
+    // the SM sub-partition. Both walk the entry records in order. S_{j+NSB}
+    // reuses the TMEM buffer of P_j and is issued once PV_j has completed.
+    const bool leader = elect_one();
+    if (warp == 2) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
+      uint32_t nq[2] = {0u, 0u};  // units per Q buffer whose S MMAs began
+      bool ok = true;
+      for (uint32_t j = 0; ok; ++j) {
+        EntryRec e;
+        ok = __all_sync(0xffffffffu, wait_entry(meta, META, j, e, abort_flag, p.err));
+        if (!ok || (e.info & kEntEnd)) break;
+        const int qb = (e.info & kEntQbuf) ? 1 : 0;
+        const int b = (int)(j % NSB);
+        if (j >= (uint32_t)NSB) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((j / NSB) - 1) & 1, abort_flag, p.err));
+        if (ok && (e.info & kEntFirst)) ok = __all_sync(0xffffffffu, mbar_wait(&q_full[qb], nq[qb] & 1, abort_flag, p.err));
+        const int s = (int)(j % NK);
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&k_full[s], (j / NK) & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t qd = smem_desc(smem_u32(smem + C::OFF_Q + qb * C::Q_BYTES), 16, 8 * ROWB, C::SWZ);
+        const uint64_t kd = smem_desc(smem_u32(smem + C::OFF_K + s * C::KV_BYTES), 16, 8 * ROWB, C::SWZ);
+        const uint32_t dS = tbase + C::s_col(b);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int c = kk / (C::CH / 16), w = kk % (C::CH / 16);
+            // descriptor start addresses advance in 16-byte units
+            umma_ss(dS, qd + (uint64_t)((c * 128 * ROWB + w * 32) >> 4), kd + (uint64_t)((c * BN * ROWB + w * 32) >> 4),
+                    IDESC_S, kk > 0);
+          }
+          umma_commit(&s_full[b]);
+          umma_commit(&k_empty[s]);
+          if (e.info & kEntLast) umma_commit(&q_empty[qb]);  // the unit's last read of its Q buffer
+        }
+        if (e.info & kEntLast) ++nq[qb];
+        __syncwarp();
+      }
+      if (leader) {
+        umma_commit(&drain[0]);  // every MMA of this thread done before TMEM is released
+        mbar_wait_drain(&drain[0], 0, p.err);
+      }
+    } else {
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
+      uint32_t units = 0u;  // units whose PV MMAs began
+      bool ok = true;
+      for (uint32_t j = 0; ok; ++j) {
+        EntryRec e;
+        ok = __all_sync(0xffffffffu, wait_entry(meta, META, j, e, abort_flag, p.err));
+        if (!ok || (e.info & kEntEnd)) break;
+        const int b = (int)(j % NSB);
+        const int sv = (int)(j % NV);
+        const bool first = (e.info & kEntFirst) != 0u;
+        ok = __all_sync(0xffffffffu, mbar_wait(&p_full[b], (j / NSB) & 1, abort_flag, p.err));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&v_full[sv], (j / NV) & 1, abort_flag, p.err));
+        // the epilogue has read the previous unit's O out of TMEM
+        if (ok && first && units > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_free, (units - 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t vd = smem_desc(smem_u32(smem + C::OFF_V + sv * C::KV_BYTES), BN * ROWB, 8 * ROWB, C::SWZ);
+        const uint32_t aP = tbase + C::s_col(b);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_ts(tbase + C::O_COL, aP + kk * 8, vd + (uint64_t)((kk * 16 * ROWB) >> 4), IDESC_O,
+                    (first && kk == 0) ? 0u : 1u);
+          umma_commit(&v_empty[sv]);
+          umma_commit(&pv_done[b]);
+          if (e.info & kEntLast) umma_commit(o_final);
+          st_release_smem(pv_issued, j + 1u);
+        }
+        if (e.info & kEntLast) ++units;
+        __syncwarp();
+      }
+      if (leader) {
+        umma_commit(&drain[1]);
+        mbar_wait_drain(&drain[1], 0, p.err);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 12) {
     // ------------------------------------------------------------ softmax
-    const int i = (warp - 4) >> 2;
+    const int h = (warp - 4) >> 2;       // which half of the key columns
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
+    const int r = quarter * 32 + lane;   // row within the query tile = TMEM lane
     const uint32_t trow = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t tS = trow + C::s_col(i);
-    const uint32_t tO = trow + C::o_col(i);
     const float sl2 = p.scale_log2;
     const bool want_mass = (!SPARSE) && (p.mass != nullptr);
     const int half = (BN == 64) ? (r >> 6) : 0;
-    float* part = reinterpret_cast<float*>(smem + C::OFF_PART) + i * 4 * C::MAX_NB;
-    uint32_t n_s = 0;   // S tiles consumed (s_full phases)
-    uint32_t nq = 0;    // units processed (o_final phases)
-    bool ok = true;
-    int ci = 0;
-    while (ok) {
-      const int id = ring_take(ci, true);
-      if (id == -1) break;
-      if (id < 0) continue;
-      Unit u;
-      decode(id, u);
-      if (i == 1 && !u.has1) continue;
-      const int bh = u.bh;
-      const int t = u.tile[i];
-      const int qpos = t * 128 + r;
-      const bool row_valid = qpos < p.n;
-      float* lam = want_mass ? p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + r : nullptr;
-
-      TileCursor cur;
-      make_cursor(cur, u, i);
-      // l: fp32 row sum (for LSE and the block masses); lt: sum of the
-      // bf16-rounded P that the tensor core multiplies (normalises O, so the
-      // output is an exact weighted mean of the rounded weights)
-      float m_ref = -INFINITY, l = 0.f, lt = 0.f;
-      uint32_t cnt = 0;
-      int32_t blk;
-      uint32_t mask;
-      while (cur.next(blk, mask)) {
-        ok = mbar_wait(&s_full[i], n_s & 1, abort_flag, p.err);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        ++n_s;
+    constexpr int NC = C::HB / 32;       // 32-column chunks per half row
+    constexpr int DH = D / 2;            // O columns this warpgroup rescales
+    float m_ref = -INFINITY, l = 0.f, lt = 0.f;
+    uint32_t cnt = 0, su = 0;
+    int t = 0, bh = 0;
+    float* lam = nullptr;
+    for (uint32_t j = 0;; ++j) {
+      EntryRec e;
+      bool ok = wait_entry(meta, META, j, e, abort_flag, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+      // every thread reads the same record; the end is taken after the
+      // exchange barrier below so that all 256 threads leave together
+      const bool end = ok && (e.info & kEntEnd);
+      const int b = (int)(j % NSB);
+      if (ok && !end) ok = mbar_wait(&s_full[b], (j / NSB) & 1, abort_flag, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok && !end && (e.info & kEntFirst)) {
+        bh = (int)e.unit / p.n_qtiles;
+        t = (int)e.unit % p.n_qtiles;
+        m_ref = -INFINITY;
+        l = 0.f;
+        lt = 0.f;
+        cnt = 0;
+        lam = want_mass ? p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + h * 128 + r : nullptr;
+      }
+      const uint32_t tS = trow + C::s_col(b);
+      uint32_t s[NC][32];
+      float mxh = -INFINITY;
+      int limit = -1;
+      if (ok && !end) {
         tc_fence_after();
-        // Dense steps: only one softmax warpgroup computes at a time, so the
-        // other stream's MMAs run while this one works (ping-pong) and the two
-        // never split the SM's issue slots. (Sparse steps, whose two streams
-        // often have different blocks, run faster without the lock.)
-        if (!SPARSE) {
-          if (r == 0) {
-            for (;;) {
-              if (*reinterpret_cast<volatile int*>(sm_lock) == 0 && atomicCAS(sm_lock, 0, 1) == 0) break;
-              __nanosleep(20);
-            }
-          }
-          named_bar_sync(3 + i, 128);
-        }
-        const int kbase = blk * BN;
-        const bool row_on = (mask >> half) & 1u;
-        // columns c <= limit are admissible (causal mask M, working-set mask R)
-        const int limit = row_on ? ((kbase + BN - 1 > qpos) ? qpos - kbase : BN) : -1;
-        const bool full = limit >= BN - 1;
-        // The whole S row (BN columns) is read from TMEM once; the row max and
-        // then P are computed from registers.
-        uint32_t s[BN / 32][32];
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld_x32(tS + cc * 32, s[cc]);
+        for (int cc = 0; cc < NC; ++cc) tmem_ld_x32(tS + h * C::HB + cc * 32, s[cc]);
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) tmem_wait_ld(s[cc]);
-        if (!full) {
+        for (int cc = 0; cc < NC; ++cc) tmem_wait_ld(s[cc]);
+        const int kbase = (int)(e.info >> 8) * BN;
+        const int qpos = t * 128 + r;
+        const bool row_on = (e.info >> (4 + half)) & 1u;
+        // columns c <= limit of the tile are admissible (causal mask M, working-set mask R)
+        limit = row_on ? ((kbase + BN - 1 > qpos) ? qpos - kbase : BN) : -1;
+        if (limit < h * C::HB + C::HB - 1) {
 #pragma unroll
-          for (int cc = 0; cc < BN / 32; ++cc)
+          for (int cc = 0; cc < NC; ++cc)
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              s[cc][j] = (cc * 32 + j <= limit) ? s[cc][j] : __float_as_uint(-INFINITY);
+            for (int q = 0; q < 32; ++q)
+              s[cc][q] = (h * C::HB + cc * 32 + q <= limit) ? s[cc][q] : __float_as_uint(-INFINITY);
         }
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc)
+        for (int cc = 0; cc < NC; ++cc)
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            mx4[j & 3] = fmax3(mx4[j & 3], __uint_as_float(s[cc][2 * j]), __uint_as_float(s[cc][2 * j + 1]));
-        float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * sl2;
-        float factor = 1.f;
-        bool resc = false;
-        if (cnt == 0) {
-          m_ref = mx;
-        } else if (mx > m_ref + 8.f) {
-          factor = fast_exp2(m_ref - mx);
-          m_ref = mx;
-          resc = true;
-        }
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // P = 2^(s*scale*log2e - m) as bf16 pairs, written over S. Packed f32x2
-        // FMA for the exponent argument, a packed add for the fp32 row sum and
-        // mixed bf16+f32 adds for the sum of the rounded P (two independent
-        // accumulators each). Masked entries hold -inf and give exactly 0.
-        const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
-        uint64_t rs2[2] = {0ull, 0ull}, rt2[2] = {0ull, 0ull};
+          for (int q = 0; q < 16; ++q)
+            mx4[q & 3] = fmax3(mx4[q & 3], __uint_as_float(s[cc][2 * q]), __uint_as_float(s[cc][2 * q + 1]));
+        mxh = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
+      } else if (lane == 0) {
+        atomicMin(sm_abort, (int)j);
+      }
+      // both halves' loads of S are complete before either writes P over it
+      tc_fence_before();
+      xch[(j & 1) * 256 + h * 128 + r] = mxh;
+      named_bar_sync(1, 256);
+      if (end || *reinterpret_cast<volatile int*>(sm_abort) <= (int)j) break;
+      tc_fence_after();
+      const float mx = fmaxf(mxh, xch[(j & 1) * 256 + (1 - h) * 128 + r]) * sl2;
+      float factor = 1.f;
+      bool resc = false;
+      if (cnt == 0) {
+        m_ref = mx;
+      } else if (mx > m_ref + 8.f) {
+        factor = fast_exp2(m_ref - mx);
+        m_ref = mx;
+        resc = true;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // P = 2^(s*scale*log2e - m) as bf16 pairs, written over S. Packed f32x2
+      // FMA for the exponent argument, a packed add for the fp32 row sum and
+      // mixed bf16+f32 adds for the sum of the rounded P (two independent
+      // accumulators each). Masked entries hold -inf and give exactly 0.
+      const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
+      uint64_t rs2[2] = {0ull, 0ull}, rt2[2] = {0ull, 0ull};
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t pk[16];
+      for (int cc = 0; cc < NC; ++cc) {
+        uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float e0, e1;
-            f2_unpack(ffma2(f2_pack(__uint_as_float(s[cc][2 * j]), __uint_as_float(s[cc][2 * j + 1])), sc2, nm2),
-                      e0, e1);
-            const float p0 = fast_exp2(e0);
-            const float p1 = fast_exp2(e1);
-            pk[j] = pack_bf16x2(p0, p1);
-            rs2[j & 1] = fadd2(rs2[j & 1], f2_pack(p0, p1));
-            add_bf16x2_to(rt2[j & 1], pk[j]);
-          }
-          tmem_st_x16(tS + cc * 16, pk);
+        for (int q = 0; q < 16; ++q) {
+          float e0, e1;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(s[cc][2 * q]), __uint_as_float(s[cc][2 * q + 1])), sc2, nm2), e0,
+                    e1);
+          const float p0 = fast_exp2(e0);
+          const float p1 = fast_exp2(e1);
+          pk[q] = pack_bf16x2(p0, p1);
+          rs2[q & 1] = fadd2(rs2[q & 1], f2_pack(p0, p1));
+          add_bf16x2_to(rt2[q & 1], pk[q]);
         }
-        float rs, rt;
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(fadd2(rs2[0], rs2[1]), a0, a1);
-          f2_unpack(fadd2(rt2[0], rt2[1]), b0, b1);
-          rs = a0 + a1;
-          rt = b0 + b1;
+        tmem_st_x16(tS + h * (C::HB / 2) + cc * 16, pk);
+      }
+      float rs, rt;
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(fadd2(rs2[0], rs2[1]), a0, a1);
+        f2_unpack(fadd2(rt2[0], rt2[1]), b0, b1);
+        rs = a0 + a1;
+        rt = b0 + b1;
+      }
+      l = l * factor + rs;
+      lt = lt * factor + rt;
+      if (__any_sync(0xffffffffu, resc)) {
+        // O of this unit holds PV up to entry j-1: wait for the last one
+        const uint32_t jb = j - 1u;
+        bool okw = mbar_wait(&pv_done[jb % NSB], (jb / NSB) & 1, abort_flag, p.err);
+        okw = __all_sync(0xffffffffu, okw);
+        if (okw) {
+          tc_fence_after();
+          rescale_o(trow + C::O_COL + h * DH, DH, factor);
+        } else if (lane == 0) {
+          atomicMin(sm_abort, (int)j + 1);
         }
-        l = l * factor + rs;
-        lt = lt * factor + rt;
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld_x32(tO + cc * 32, o);
-            tmem_wait_ld(o);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
-            tmem_st_x32(tO + cc * 32, o);
-          }
+      }
+      tmem_wait_st();
+      if (want_mass) lam[(size_t)cnt * 256] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[b]);
+      ++cnt;
+      if (e.info & kEntLast) {
+        // per-row statistics of the unit for the epilogue
+        const int sb = (int)(su & 1);
+        bool okw = (su < 2) || mbar_wait(&st_empty[sb], ((su >> 1) - 1) & 1, abort_flag, p.err);
+        okw = __all_sync(0xffffffffu, okw);
+        if (okw) {
+          float* st = stats + sb * 5 * 128;
+          if (h == 0) st[r] = m_ref;
+          st[(1 + h) * 128 + r] = l;
+          st[(3 + h) * 128 + r] = lt;
         }
-        tmem_wait_st();
-        if (!SPARSE) {
-          named_bar_sync(3 + i, 128);
-          if (r == 0) atomicExch(sm_lock, 0);
-        }
-        if (want_mass) lam[(size_t)cnt * 128] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[i]);
-        ++cnt;
+        if (lane == 0) {
+          if (okw) mbar_arrive(&st_full[sb]);
+          else atomicMin(sm_abort, (int)j + 1);
+        }
+        ++su;
       }
-
-      // ------------------------------------------------------------ epilogue
-      if (ok) {  // the unit's MMAs are complete (waited even without entries: keeps phases in step)
-        ok = mbar_wait(&o_final[i], nq & 1, abort_flag, p.err);
-        ok = __all_sync(0xffffffffu, ok);
-        ++nq;
-        tc_fence_after();
-      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t tO = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + C::O_COL;
+    const bool want_mass = (!SPARSE) && (p.mass != nullptr);
+    uint32_t eu = 0;  // units with entries processed (o_final / stats phases)
+    for (int u = 0;; ++u) {
+      const int slot = u % URING;
+      bool ok = mbar_wait(&u_full[slot], (u / URING) & 1, abort_flag, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+      int id = -1, cnt = 0;
       if (ok) {
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const float inv_l = (lt > 0.f) ? 1.f / lt : 0.f;
-        const size_t grow = (size_t)bh * p.n + qpos;
+        id = uring[2 * slot];
+        cnt = uring[2 * slot + 1];
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&u_empty[slot]);
+      const bool end = ok && id < 0;  // every epilogue thread reads the same record
+      if (end) cnt = 0;
+      const int bh = ok ? id / p.n_qtiles : 0, t = ok ? id % p.n_qtiles : 0;
+      const int qpos = t * 128 + r;
+      const bool row_valid = qpos < p.n;
+      const size_t grow = (size_t)bh * p.n + qpos;
+      float m = 0.f, lsum = 0.f, ltsum = 0.f;
+      if (ok && cnt > 0) {
+        const int sb = (int)(eu & 1);
+        ok = mbar_wait(&st_full[sb], (eu >> 1) & 1, abort_flag, p.err);
+        if (ok) {
+          const float* st = stats + sb * 5 * 128;
+          m = st[r];
+          lsum = st[128 + r] + st[256 + r];
+          ltsum = st[384 + r] + st[512 + r];
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&st_empty[sb]);
+        if (ok) ok = mbar_wait(o_final, eu & 1, abort_flag, p.err);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (!ok && lane == 0) atomicMin(ep_abort, u);
+      named_bar_sync(2, 128);
+      if (end || *reinterpret_cast<volatile int*>(ep_abort) <= u) break;
+      const float inv_l = (ltsum > 0.f) ? 1.f / ltsum : 0.f;
+      if (cnt > 0) tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          if (cnt > 0) {
-            tmem_ld_x32(tO + cc * 32, o);
-            tmem_wait_ld(o);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = 0u;
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        if (cnt > 0) {
+          tmem_ld_x32(tO + cc * 32, o);
+          tmem_wait_ld(o);
+          if (cc == D / 32 - 1) {
+            // O is out of TMEM: the next unit's PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
           }
-          if (row_valid) {
-            if (p.out_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + grow * D + cc * 32);
+        } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv_l, __uint_as_float(o[4 * j + 1]) * inv_l,
-                                     __uint_as_float(o[4 * j + 2]) * inv_l, __uint_as_float(o[4 * j + 3]) * inv_l);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D + cc * 32);
+          for (int q = 0; q < 32; ++q) o[q] = 0u;
+        }
+        if (row_valid) {
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + grow * D + cc * 32);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(o[8 * j + 0]) * inv_l, __uint_as_float(o[8 * j + 1]) * inv_l);
-                v.y = pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv_l, __uint_as_float(o[8 * j + 3]) * inv_l);
-                v.z = pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv_l, __uint_as_float(o[8 * j + 5]) * inv_l);
-                v.w = pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv_l, __uint_as_float(o[8 * j + 7]) * inv_l);
-                dst[j] = v;
-              }
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                   __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D + cc * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+              dst[q] = v;
             }
           }
         }
-        const float lse2 = (l > 0.f) ? m_use + fast_log2(l) : -INFINITY;
-        if (p.lse != nullptr && row_valid) p.lse[grow] = lse2 * 0.69314718055994531f;
-        if (want_mass) {
-          // Eq 5: r_qb = (1/B) sum over the block's rows of 2^(lam_ib - lse2_i).
-#pragma unroll 1
-          for (uint32_t e = 0; e < cnt; ++e) {
-            float a = (row_valid && l > 0.f) ? fast_exp2(lam[(size_t)e * 128] - lse2) : 0.f;
+      }
+      const float lse2 = (lsum > 0.f) ? m + fast_log2(lsum) : -INFINITY;
+      if (p.lse != nullptr && row_valid) p.lse[grow] = lse2 * 0.69314718055994531f;
+      if (want_mass) {
+        // Eq 5: r_qb = (1/B) * sum over the block's rows of 2^(lam_ib - lse2_i),
+        // lam summed over the two column halves. Entries go through `part`
+        // 64 at a time; blocks past the unit's entries are zero.
+        const float* lam = p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + r;
+        for (int c0 = 0; c0 < cnt; c0 += 64) {
+          const int c1 = min(cnt, c0 + 64);
+          for (int e = c0; e < c1; ++e) {
+            float a = 0.f;
+            if (row_valid && lsum > 0.f)
+              a = fast_exp2(lam[(size_t)e * 256] - lse2) + fast_exp2(lam[(size_t)e * 256 + 128] - lse2);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            if (lane == 0) part[quarter * p.nb + e] = a;
+            if (lane == 0) part[quarter * 64 + (e - c0)] = a;
           }
-          named_bar_sync(1 + i, 128);
-          constexpr int QB_PER_TILE = C::ENT_PER_TILE;
-          for (int qq = 0; qq < QB_PER_TILE; ++qq) {
-            const int qb = t * QB_PER_TILE + qq;
-            if (qb >= p.nb) break;
-            float* dst = p.mass + ((size_t)bh * p.nb + qb) * p.nb;
-            for (int e = r; e < p.nb; e += 128) {
-              float v = 0.f;
-              if (e < (int)cnt) {
-                if (BN == 128) {
-                  v = (part[0 * p.nb + e] + part[1 * p.nb + e]) + (part[2 * p.nb + e] + part[3 * p.nb + e]);
-                } else {
-                  v = part[(2 * qq) * p.nb + e] + part[(2 * qq + 1) * p.nb + e];
-                }
-                v *= (1.f / BN);
+          named_bar_sync(2, 128);
+          const int e = c0 + (r & 63);
+          if (e < c1) {
+            if (BN == 128) {
+              if (r < 64) {
+                const float v = (part[e - c0] + part[64 + e - c0]) + (part[128 + e - c0] + part[192 + e - c0]);
+                p.mass[((size_t)bh * p.nb + t) * p.nb + e] = v * (1.f / BN);
               }
-              dst[e] = v;
+            } else {
+              const int qq = r >> 6;
+              const int qb = 2 * t + qq;
+              if (qb < p.nb) {
+                const float v = part[(2 * qq) * 64 + e - c0] + part[(2 * qq + 1) * 64 + e - c0];
+                p.mass[((size_t)bh * p.nb + qb) * p.nb + e] = v * (1.f / BN);
+              }
             }
           }
-          named_bar_sync(1 + i, 128);  // partials are reused by the next unit
+          named_bar_sync(2, 128);  // part is reused by the next chunk
+        }
+        for (int qq = 0; qq < C::ENT_PER_TILE; ++qq) {
+          const int qb = t * C::ENT_PER_TILE + qq;
+          if (qb >= p.nb) break;
+          float* dst = p.mass + ((size_t)bh * p.nb + qb) * p.nb;
+          for (int e = cnt + r; e < p.nb; e += 128) dst[e] = 0.f;
         }
       }
+      if (cnt > 0) ++eu;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 3) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }

@@ -10,15 +10,14 @@ struct AttnParams {
   int32_t bh_count;     // batch * heads
   int32_t n;            // sequence length
   int32_t nb;           // n / BN key (and query) blocks
-  int32_t n_qtiles;     // ceil(n / 128)
-  int32_t npairs;       // ceil(n_qtiles / 2): work units per (batch, head)
+  int32_t n_qtiles;     // ceil(n / 128): work units (query tiles) per (batch, head)
   int32_t group_heads;  // (batch, head) slices per L2 group in the default order
   float scale_log2;     // softmax scale * log2(e)
   int32_t out_f32;      // O dtype: 0 bf16, 1 f32
   void* o;
   float* lse;           // optional
   float* mass;          // optional [bh, nb, nb] (discover only)
-  float* lam;           // per-row per-entry log2-sum-exp scratch (mass only)
+  float* lam;           // per-row, per-entry, per-half log2-sum-exp scratch (mass only)
   const int32_t* row_ptr;
   const int32_t* col_idx;
   int64_t col_cap;
@@ -40,7 +39,7 @@ struct SelectLaunch {
   int64_t col_cap;
   int32_t* nnz;
   int32_t* tile_order;
-  int32_t npairs, qb_per_unit, group_heads;
+  int32_t units_per_bh, qb_per_unit, group_heads;
   uint32_t* err;
 };
 

@@ -40,8 +40,8 @@ struct SelectParams {
   int64_t col_cap;
   int32_t* nnz;
   int32_t* tile_order;
-  int32_t npairs;
-  int32_t qb_per_unit;  // query blocks per work unit (256 / block)
+  int32_t units_per_bh;
+  int32_t qb_per_unit;  // query blocks per work unit (128 / block)
   int32_t group_heads;
   uint32_t* err;
 };
@@ -161,9 +161,9 @@ constexpr int kChunkRows = 256;  // rows per finalize CTA (one per thread)
 __device__ void order_group(const SelectParams& p, int g, int32_t* cost) {
   const int h0 = g * p.group_heads;
   const int gsize = min(p.group_heads, p.bh_count - h0);
-  const int units = gsize * p.npairs;
+  const int units = gsize * p.units_per_bh;
   for (int u = threadIdx.x; u < units; u += blockDim.x) {
-    const int bh = h0 + u / p.npairs, pr = u % p.npairs;
+    const int bh = h0 + u / p.units_per_bh, pr = u % p.units_per_bh;
     int c = 0;
     for (int j = 0; j < p.qb_per_unit; ++j) {
       const int qb = pr * p.qb_per_unit + j;
@@ -172,7 +172,7 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* cost) {
     cost[u] = c;
   }
   __syncthreads();
-  const int64_t gbase = (int64_t)h0 * p.npairs;
+  const int64_t gbase = (int64_t)h0 * p.units_per_bh;
   for (int u = threadIdx.x; u < units; u += blockDim.x) {
     const int c = cost[u];
     int pos = 0;
@@ -180,7 +180,7 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* cost) {
       const int cv = cost[v];
       pos += (cv > c || (cv == c && v < u)) ? 1 : 0;
     }
-    p.tile_order[gbase + pos] = h0 * p.npairs + u;
+    p.tile_order[gbase + pos] = h0 * p.units_per_bh + u;
   }
 }
 
@@ -273,7 +273,7 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   p.col_cap = s.col_cap;
   p.nnz = s.nnz;
   p.tile_order = s.tile_order;
-  p.npairs = s.npairs;
+  p.units_per_bh = s.units_per_bh;
   p.qb_per_unit = s.qb_per_unit;
   p.group_heads = s.group_heads;
   p.err = s.err;
@@ -288,7 +288,7 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   else select_rows_kernel<32><<<grid_rows, 256, 0, stream>>>(p);
   const int n_chunks = (int)((rows + kChunkRows - 1) / kChunkRows);
   const int groups = s.tile_order ? (s.bh_count + s.group_heads - 1) / s.group_heads : 0;
-  const size_t shm = s.tile_order ? (size_t)s.group_heads * s.npairs * sizeof(int32_t) : 0;
+  const size_t shm = s.tile_order ? (size_t)s.group_heads * s.units_per_bh * sizeof(int32_t) : 0;
   if (shm > 40 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
     if (e != cudaSuccess) return e;

@@ -94,7 +94,7 @@ int check_desc(const wise_attn_desc* d) {
 
 struct Shape {
   int64_t bh;
-  int n, d, bn, nb, n_qtiles, npairs, group_heads;
+  int n, d, bn, nb, n_qtiles, group_heads;
   int64_t n_units;
 };
 
@@ -106,20 +106,19 @@ Shape shape_of(const wise_attn_desc* d) {
   s.bn = d->block;
   s.nb = d->seq_len / d->block;
   s.n_qtiles = (d->seq_len + 127) / 128;
-  s.npairs = (s.n_qtiles + 1) / 2;
   const size_t kv_per_head = (size_t)2 * d->seq_len * d->head_dim * 2;
   int64_t g = (int64_t)(kL2GroupBytes / kv_per_head);
   if (g < 1) g = 1;
   if (g > s.bh) g = s.bh;
   s.group_heads = (int)g;
-  s.n_units = s.bh * s.npairs;
+  s.n_units = s.bh * s.n_qtiles;
   return s;
 }
 
 size_t lam_bytes(const Shape& s) {
   const int64_t ept = 128 / s.bn;
   const int64_t per_bh = ept * (int64_t)s.n_qtiles * (s.n_qtiles + 1) / 2;
-  return (size_t)(s.bh * per_bh * 128 * sizeof(float));
+  return (size_t)(s.bh * per_bh * 256 * sizeof(float));
 }
 
 int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -140,7 +139,6 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
   p.n = s.n;
   p.nb = s.nb;
   p.n_qtiles = s.n_qtiles;
-  p.npairs = s.npairs;
   p.group_heads = s.group_heads;
   const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / sqrtf((float)s.d);
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -301,8 +299,8 @@ int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int
   sl.col_cap = col_capacity;
   sl.nnz = nnz;
   sl.tile_order = tile_order;
-  sl.npairs = s.npairs;
-  sl.qb_per_unit = 256 / s.bn;
+  sl.units_per_bh = s.n_qtiles;
+  sl.qb_per_unit = 128 / s.bn;
   sl.group_heads = s.group_heads;
   sl.err = err;
   cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
@@ -344,8 +342,8 @@ int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_m
   sl.col_cap = col_capacity;
   sl.nnz = nnz;
   sl.tile_order = tile_order;
-  sl.npairs = s.npairs;
-  sl.qb_per_unit = 256 / s.bn;
+  sl.units_per_bh = s.n_qtiles;
+  sl.qb_per_unit = 128 / s.bn;
   sl.group_heads = s.group_heads;
   sl.err = err;
   cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));

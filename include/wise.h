@@ -111,7 +111,7 @@ int wise_attn_discover(const wise_attn_desc* desc, const void* q, const void* k,
                        size_t workspace_bytes, wise_stream_t stream);
 
 /* Number of work units of the late-step kernel: the length of the
- * tile_order schedule (one unit = 256 consecutive query rows of one
+ * tile_order schedule (one unit = 128 consecutive query rows of one
  * (batch, head)); 0 when the descriptor is invalid. */
 int64_t wise_schedule_units(const wise_attn_desc* desc);
 

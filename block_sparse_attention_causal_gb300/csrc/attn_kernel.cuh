@@ -8,25 +8,30 @@
 //    §5.2 Eqs 7-8 -- only listed key blocks are loaded and multiplied.
 //
 // Persistent: one CTA per SM pulls work units (one 128-row query tile of one
-// (batch, head)) from the work order, heaviest first. The key blocks of all
-// units a CTA takes form one continuous stream of "entries"; the pipeline runs
-// across unit boundaries. Warp roles (512 threads, four warpgroups):
-//   warp 0      scheduler: claims units, walks their key-block lists, and
-//               publishes one record per entry in a shared-memory ring
-//   warp 1      TMA loads of Q (once per unit), K (ring of NK slots) and V
-//               (ring of NV slots)
-//   warp 2      issues the S = Q K^T MMAs (one elected lane)
-//   warp 3      TMEM allocator; issues the O += P V MMAs (one elected lane)
-//   warps 4-7   softmax warpgroup 0: key columns [0, BN/2) of every row
-//   warps 8-11  softmax warpgroup 1: key columns [BN/2, BN)
-//   warps 12-15 epilogue: O normalisation and store, LSE, block masses
-// TMEM holds three S buffers and the O accumulator. S for entry j+1 and j+2
-// is computed while the softmax works on entry j; P (bf16) is written over
-// S_j and consumed from TMEM by the PV MMA, after which S_{j+3} reuses the
-// buffer. The two softmax warpgroups split each score row and exchange row
-// maxima through shared memory. The running row max is only moved (and O
-// rescaled) when it grows by more than 2^8, so most entries skip the O
-// correction.
+// (batch, head)) from the work order, heaviest first. Each CTA runs two
+// independent query-tile streams; while the softmax of one stream works on its
+// scores, the tensor core runs the other stream's MMAs. The key blocks
+// ("entries") of both streams are published in one record ring, alternating
+// between the streams while both have work.
+//
+// Warp roles (512 threads, four warpgroups):
+//   warp 0      scheduler: claims units, walks their key-block lists and
+//               publishes one record per entry (plus an end marker per stream)
+//   warp 1      TMA loads of Q (per unit, one buffer per stream), K and V
+//   warp 2      issues every MMA from one thread: for each record in order,
+//               O_s += P_s V, then S_s = Q_s K^T of that stream's next entry
+//   warp 3      TMEM allocation
+//   warps 4-7   softmax of stream 0, one score row per thread
+//   warps 8-11  softmax of stream 1
+//   warps 12-15 epilogue of both streams: O normalisation and store, LSE,
+//               block masses
+// TMEM: S_0 | S_1 | O_0 | O_1. P (bf16) is written over S_s by the softmax
+// and read from TMEM by the PV MMA; the next S_s of the same stream is issued
+// by the same thread right after that PV MMA, and tcgen05 MMAs issued by one
+// thread execute in issue order. The commit that signals S_s also covers
+// every earlier MMA, so when the softmax sees S_s its O_s already holds all
+// previous entries and can be rescaled in place. The running row max only
+// moves (and O is rescaled) when it grows by more than 2^8.
 #pragma once
 #include <stdint.h>
 
@@ -45,14 +50,14 @@ struct SchedSlot {
 constexpr int kSchedSlots = 256;
 static __device__ SchedSlot g_sched[kSchedSlots];
 
-// Flags of an entry record.
+// Flags of an entry record (low byte of `info`; the key block index is above).
 enum : uint32_t {
   kEntFirst = 1u,   // first entry of its unit
   kEntLast = 2u,    // last entry of its unit
-  kEntEnd = 4u,     // no more entries: the CTA's work is done
-  kEntQbuf = 8u,    // Q buffer of the unit
-  kEntRows0 = 16u,  // the rows of query block 0 of the tile list this key block
-  kEntRows1 = 32u,  // ... of query block 1 (BN = 64 only)
+  kEntMark = 4u,    // end marker: the stream has no more entries
+  kEntStream = 8u,  // the record belongs to stream 1 (else stream 0)
+  kEntRows0 = 16u,  // query block 0 of the tile lists this key block
+  kEntRows1 = 32u,  // ... query block 1 (BN = 64 only)
 };
 
 template <int D, int BN, bool SPARSE>
@@ -66,44 +71,35 @@ struct AttnCfg {
   static constexpr uint32_t Q_BYTES = 128u * D * 2u;
   static constexpr uint32_t KV_BYTES = (uint32_t)BN * D * 2u;
   static constexpr int THREADS = 512;
-  static constexpr int NSB = 3;       // S buffers in TMEM
   static constexpr int META = 32;     // entry records in flight
-  static constexpr int URING = 8;     // unit records in flight (epilogue)
-  static constexpr int HB = BN / 2;   // key columns per softmax warpgroup
   static constexpr int MAX_NB = 1024;
   static constexpr int ENT_PER_TILE = 128 / BN;  // query blocks per 128-row tile
-  // shared memory: Q[2] | K[NK] | V[NV] | xch | stats | part | meta | units | barriers | misc
-  static constexpr uint32_t XCH_BYTES = 2u * 2u * 128u * 4u;    // row-max exchange, two tiles
-  static constexpr uint32_t STATS_BYTES = 2u * 5u * 128u * 4u;  // per-row m, l, lt of two units
-  static constexpr uint32_t PART_BYTES = SPARSE ? 0u : 4u * 64u * 4u;
+  // per stream: lse2[128], inv_l[128], unit, entries (+ padding)
+  static constexpr int ST_STRIDE = 2 * 128 + 8;
+  static constexpr uint32_t STATS_BYTES = 2u * ST_STRIDE * 4u;
   static constexpr uint32_t META_BYTES = META * 16u;
-  static constexpr uint32_t URING_BYTES = URING * 8u;
-  static constexpr int NBAR_FIXED = 2 + 2 + 3 * NSB + 2 + 2 + 2 + 2 * URING + 2;
+  static constexpr int NBAR_FIXED = 8 * 2 + 2 + 8;
+  static constexpr uint32_t MISC_BYTES = 64;
   static constexpr uint32_t SMEM_LIMIT = 232448u;  // 227 KB per CTA
-  static constexpr uint32_t FIXED = 2u * Q_BYTES + XCH_BYTES + STATS_BYTES + PART_BYTES + META_BYTES + URING_BYTES +
-                                    (NBAR_FIXED + 16) * 8u + 32u + 1024u;
+  static constexpr uint32_t FIXED = 2u * Q_BYTES + STATS_BYTES + META_BYTES + MISC_BYTES + (NBAR_FIXED + 16) * 8u;
   static constexpr int SLOTS_FIT = (int)((SMEM_LIMIT - FIXED) / KV_BYTES);
-  static constexpr int NK = SLOTS_FIT >= 8 ? 4 : (SLOTS_FIT + 1) / 2;
-  static constexpr int NV = SLOTS_FIT >= 8 ? 4 : SLOTS_FIT / 2;
+  static constexpr int NK = ((SLOTS_FIT + 1) / 2 > 4) ? 4 : (SLOTS_FIT + 1) / 2;
+  static constexpr int NV = (SLOTS_FIT / 2 > 4) ? 4 : SLOTS_FIT / 2;
   static_assert(NK >= 2 && NV >= 2, "K/V rings");
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2u * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + NK * KV_BYTES;
-  static constexpr uint32_t OFF_XCH = OFF_V + NV * KV_BYTES;
-  static constexpr uint32_t OFF_STATS = OFF_XCH + XCH_BYTES;
-  static constexpr uint32_t OFF_PART = OFF_STATS + STATS_BYTES;
-  static constexpr uint32_t OFF_META = OFF_PART + PART_BYTES;
-  static constexpr uint32_t OFF_URING = OFF_META + META_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_URING + URING_BYTES;
+  static constexpr uint32_t OFF_STATS = OFF_V + NV * KV_BYTES;
+  static constexpr uint32_t OFF_META = OFF_STATS + STATS_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_META + META_BYTES;
   static constexpr int NBAR = NBAR_FIXED + 2 * NK + 2 * NV;
-  // tmem base (+0), abort flag (+4), entries whose PV was issued (+8),
-  // softmax abort entry (+12), epilogue abort unit (+16)
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32u + 1024u;  // + alignment slack
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
+  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle atoms");
   static constexpr uint32_t TMEM_COLS = 512;
-  __host__ __device__ static constexpr uint32_t s_col(int b) { return 128u * (uint32_t)b; }
-  static constexpr uint32_t O_COL = 384;
+  __host__ __device__ static constexpr uint32_t s_col(int s) { return 128u * (uint32_t)s; }
+  __host__ __device__ static constexpr uint32_t o_col(int s) { return 256u + (uint32_t)(s * D); }
 };
 
 // Entries (key blocks) of one 128-row query tile in ascending order. Dense:
@@ -190,29 +186,32 @@ __device__ __forceinline__ int64_t default_unit(int64_t x, const AttnParams& p) 
   return bh * p.n_qtiles + t;
 }
 
-// First float of tile t's Eq 5 scratch: per entry, two halves of 128 rows.
+// First float of tile t's Eq 5 scratch: per entry, one value per row.
 __device__ __forceinline__ int64_t lam_tile_offset(int bh, int t, const AttnParams& p, int ept) {
   const int64_t before = (int64_t)ept * t * (t + 1) / 2;
   const int64_t total = (int64_t)ept * p.n_qtiles * (p.n_qtiles + 1) / 2;
-  return ((int64_t)bh * total + before) * 256;
+  return ((int64_t)bh * total + before) * 128;
 }
 
+template <int TAG>
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* err) {
   int dummy_abort = 0;
-  return mbar_wait(bar, parity, &dummy_abort, err);
+  return mbar_wait<TAG>(bar, parity, &dummy_abort, err);
 }
 
-// Entry records: word 0 is the tag (entry index + 1), written last.
-struct EntryRec {
+// Entry records: word 0 is the tag (record index + 1), written last; tag and
+// info are read together with one 64-bit acquire load.
+struct __align__(16) EntryRec {
   uint32_t tag;
+  uint32_t info;   // flags | block index << 8
   uint32_t krow;   // global row of the key block's first key (TMA coordinate)
   uint32_t unit;   // unit id = bh * n_qtiles + tile
-  uint32_t info;   // flags | block index << 8
 };
 
 // Wait until record j is published; false on abort/timeout or if the ring
 // was overrun (which the scheduler's flow control rules out). The spin is out
 // of line; the common case (already published) is one load and a compare.
+template <int TAG>
 static __device__ __noinline__ bool wait_entry_slow(EntryRec* r, uint32_t j, volatile int* abort_flag, uint32_t* err) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -233,14 +232,22 @@ static __device__ __noinline__ bool wait_entry_slow(EntryRec* r, uint32_t j, vol
     }
   }
 }
+// FULL: also read krow and unit (tag and info always).
+template <int TAG, bool FULL>
 __device__ __forceinline__ bool wait_entry(EntryRec* ring, int meta, uint32_t j, EntryRec& out,
                                            volatile int* abort_flag, uint32_t* err) {
   EntryRec* r = ring + (j % (uint32_t)meta);
-  if (ld_acquire_smem(&r->tag) != j + 1u && !wait_entry_slow(r, j, abort_flag, err)) return false;
+  uint64_t ti = ld_acquire_smem_b64(&r->tag);
+  if ((uint32_t)ti != j + 1u) {
+    if (!wait_entry_slow<TAG>(r, j, abort_flag, err)) return false;
+    ti = ld_acquire_smem_b64(&r->tag);
+  }
   out.tag = j + 1u;
-  out.krow = r->krow;
-  out.unit = r->unit;
-  out.info = r->info;
+  out.info = (uint32_t)(ti >> 32);
+  if (FULL) {
+    out.krow = r->krow;
+    out.unit = r->unit;
+  }
   return true;
 }
 
@@ -264,79 +271,110 @@ static __device__ __noinline__ void rescale_o(uint32_t tO, int ncols, float fact
   }
 }
 
+// Output rows of a unit with no entries (a sparse tile whose query blocks list
+// nothing): O = 0 and LSE = -inf.
+static __device__ __noinline__ void write_empty_unit(int id, const AttnParams& p, int d) {
+  const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
+  for (int rr = 0; rr < 128; ++rr) {
+    const int qpos = t * 128 + rr;
+    if (qpos >= p.n) break;
+    const size_t grow = (size_t)bh * p.n + qpos;
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + grow * d);
+      for (int c = 0; c < d / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * d);
+      for (int c = 0; c < d / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (p.lse != nullptr) p.lse[grow] = -INFINITY;
+  }
+}
+
+__device__ __forceinline__ void sched_slot_done(const AttnParams& p) {
+  // every CTA has pulled its last position: the last one out resets the slot
+  __threadfence();
+  if (atomicAdd(&g_sched[p.sched_slot].done, 1u) == gridDim.x - 1) {
+    g_sched[p.sched_slot].next = 0u;
+    g_sched[p.sched_slot].done = 0u;
+    __threadfence();
+  }
+}
+
 template <int D, int BN, bool SPARSE>
 __global__ void __launch_bounds__(512, 1)
     wise_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   using C = AttnCfg<D, BN, SPARSE>;
-  constexpr int NK = C::NK, NV = C::NV, NSB = C::NSB, META = C::META, URING = C::URING;
+  constexpr int NK = C::NK, NV = C::NV, META = C::META;
   constexpr uint32_t ROWB = C::ROWB;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // 128B-swizzled TMA tiles need 1024-byte aligned destinations
+  if ((smem_u32(smem) & 1023u) != 0u) {
+    if (threadIdx.x == 0) {
+      atomicOr(p.err, kErrInternal);
+      sched_slot_done(p);
+    }
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;              // [2]
-  uint64_t* q_empty = q_full + 2;       // [2]
-  uint64_t* s_full = q_empty + 2;       // [NSB]
-  uint64_t* p_full = s_full + NSB;      // [NSB]
-  uint64_t* pv_done = p_full + NSB;     // [NSB]
-  uint64_t* o_final = pv_done + NSB;    // [1]
-  uint64_t* o_free = o_final + 1;       // [1]
-  uint64_t* st_full = o_free + 1;       // [2]
-  uint64_t* st_empty = st_full + 2;     // [2]
-  uint64_t* u_full = st_empty + 2;      // [URING]
-  uint64_t* u_empty = u_full + URING;   // [URING]
-  uint64_t* drain = u_empty + URING;    // [2]
-  uint64_t* k_full = drain + 2;         // [NK]
-  uint64_t* k_empty = k_full + NK;      // [NK]
-  uint64_t* v_full = k_empty + NK;      // [NV]
-  uint64_t* v_empty = v_full + NV;      // [NV]
+  uint64_t* q_full = bars;           // [2] Q of the stream's unit loaded
+  uint64_t* q_empty = q_full + 2;    // [2] last S MMA of the stream's unit done
+  uint64_t* s_full = q_empty + 2;    // [2] S_s computed
+  uint64_t* p_full = s_full + 2;     // [2] P_s written (4 softmax warps)
+  uint64_t* o_final = p_full + 2;    // [2] last PV MMA of the stream's unit done
+  uint64_t* o_free = o_final + 2;    // [2] O_s read out by the epilogue (4 warps)
+  uint64_t* st_full = o_free + 2;    // [2] unit statistics written (4 softmax warps)
+  uint64_t* st_empty = st_full + 2;  // [2] unit statistics consumed (4 epilogue warps)
+  uint64_t* drain = st_empty + 2;    // [2] all MMAs of issuer s done
+  uint64_t* comp_full = drain + 2;   // [8] completion word n % 8 written (phase n / 8)
+  uint64_t* k_full = comp_full + 8;  // [NK]
+  uint64_t* k_empty = k_full + NK;   // [NK]
+  uint64_t* v_full = k_empty + NK;   // [NV]
+  uint64_t* v_empty = v_full + NV;   // [NV]
   EntryRec* meta = reinterpret_cast<EntryRec*>(smem + C::OFF_META);
-  int32_t* uring = reinterpret_cast<int32_t*>(smem + C::OFF_URING);  // {unit id, entries}
-  float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
   float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS);
-  float* part = reinterpret_cast<float*>(smem + C::OFF_PART);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_base_slot = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  uint32_t* pv_issued = misc + 2;
-  int* sm_abort = reinterpret_cast<int*>(misc + 3);
-  int* ep_abort = reinterpret_cast<int*>(misc + 4);
+  uint32_t* qpos0 = misc + 2;
+  int* ep_bad = reinterpret_cast<int*>(misc + 3);
+  uint32_t* qpos1 = misc + 4;
+  uint32_t* comp_tail = misc + 5;
+  // completed units in the order their last PV MMA was issued: word n % 8 =
+  // (n + 1) << 2 | end flag << 1 | stream, announced on comp_full[n % 8]
+  uint32_t* comp = misc + 8;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
-      mbar_init(&st_full[i], 8);   // one arrival per softmax warp
-      mbar_init(&st_empty[i], 4);  // one arrival per epilogue warp
-    }
-    for (int b = 0; b < NSB; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 8);
-      mbar_init(&pv_done[b], 1);
-    }
-    mbar_init(o_final, 1);
-    mbar_init(o_free, 4);
-    for (int j = 0; j < URING; ++j) {
-      mbar_init(&u_full[j], 1);
-      mbar_init(&u_empty[j], 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&o_final[s], 1);
+      mbar_init(&o_free[s], 4);
+      mbar_init(&st_full[s], 4);
+      mbar_init(&st_empty[s], 4);
     }
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
-    for (int s = 0; s < NK; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&comp_full[i], 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
     }
-    for (int s = 0; s < NV; ++s) {
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     for (int j = 0; j < META; ++j) meta[j].tag = 0u;
     *abort_flag = 0;
-    *pv_issued = 0u;
-    *sm_abort = INT32_MAX;
-    *ep_abort = INT32_MAX;
+    *qpos0 = 0u;
+    *qpos1 = 0u;
+    *comp_tail = 0u;
+    *ep_bad = 0;
+    for (int i = 0; i < 8; ++i) comp[i] = 0u;
     fence_mbar_init();
   }
   if (warp == 3) {
@@ -347,20 +385,26 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_base_slot;
-
+  // Registers per thread: 80 (warps 0-3) + 184 (two softmax warpgroups) + 64
+  // (epilogue), in sum the 512 x 128 of the launch; each warpgroup sets its
+  // count at the top of its branch.
+  if (warp < 4) {
+  setmaxnreg_dec<80>();
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler
     if (lane == 0) {
       SchedSlot* sched = &g_sched[p.sched_slot];
-      uint32_t j = 0;  // entries published
-      int u = 0;       // units published
-      int uq = 0;      // units with at least one entry
+      uint32_t j = 0;  // records published
       bool ok = true;
-      // publish one entry record, after the flow control allows slot j
+      // Publish one record once the flow control allows slot j. qpos_s is one
+      // past the last record whose PV MMA stream s's issuer has issued; every
+      // reader (softmax, loader, issuers) is at or beyond min(qpos0, qpos1),
+      // and four slots of the ring stay out of the scheduler's reach.
+      constexpr uint32_t AHEAD = (uint32_t)META - 4u;
       auto publish = [&](uint32_t krow, uint32_t unit, uint32_t info) -> bool {
-        if (j >= (uint32_t)META) {
+        if (j >= AHEAD) {
           const uint64_t t0 = global_timer_ns();
-          for (uint32_t it = 0; j >= ld_acquire_smem(pv_issued) + (uint32_t)META; ++it) {
+          for (uint32_t it = 0; j >= min(ld_acquire_smem(qpos0), ld_acquire_smem(qpos1)) + AHEAD; ++it) {
             if ((it & 63u) == 63u) {
               if (*abort_flag) return false;
               if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -373,301 +417,361 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
         EntryRec* r = meta + (j % (uint32_t)META);
+        r->info = info;
         r->krow = krow;
         r->unit = unit;
-        r->info = info;
         st_release_smem(&r->tag, j + 1u);
         ++j;
         return true;
       };
-      while (ok) {
-        const unsigned int x = atomicAdd(&sched->next, 1u);
-        int id = -1;
-        if ((int64_t)x < p.n_units) {
+      // per-stream state in two named structs (no runtime-indexed arrays:
+      // those would live in local memory)
+      struct StreamCur {
+        TileCursor cur;
+        int unit, cnt;
+        int32_t pblk;
+        uint32_t pmask;
+        bool alive;
+      };
+      StreamCur sc0, sc1;
+      // claim the next unit with at least one entry for stream s
+      auto claim = [&](StreamCur& sc) -> bool {
+        for (;;) {
+          if (*abort_flag) return false;
+          const unsigned int x = atomicAdd(&sched->next, 1u);
+          if ((int64_t)x >= p.n_units) return false;
           const int64_t v = (SPARSE && p.tile_order != nullptr) ? (int64_t)__ldg(p.tile_order + x) : default_unit(x, p);
-          id = (v >= 0 && v < p.n_units) ? (int)v : -2;
-          if (id == -2) {
+          if (v < 0 || v >= p.n_units) {
             atomicOr(p.err, kErrBadSupport);
             continue;
           }
-        }
-        if (id == -1) break;
-        const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
-        TileCursor cur;
-        if (SPARSE) cur.init_sparse(t, bh, p, C::ENT_PER_TILE);
-        else cur.init_dense(t, p, BN);
-        const uint32_t qbuf = (uq & 1) ? kEntQbuf : 0u;
-        int cnt = 0;
-        int32_t blk, pblk = -1;
-        uint32_t mask, pmask = 0;
-        while (cur.next(blk, mask)) {
-          if (cnt > 0) {
-            const uint32_t info = (cnt == 1 ? kEntFirst : 0u) | qbuf | (pmask << 4) | ((uint32_t)pblk << 8);
-            if (!(ok = publish((uint32_t)(bh * p.n + pblk * BN), (uint32_t)id, info))) break;
+          const int id = (int)v;
+          const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
+          if (SPARSE) sc.cur.init_sparse(t, bh, p, C::ENT_PER_TILE);
+          else sc.cur.init_dense(t, p, BN);
+          if (!sc.cur.next(sc.pblk, sc.pmask)) {
+            if (sc.cur.bad) atomicOr(p.err, kErrBadSupport);
+            write_empty_unit(id, p, D);
+            continue;
           }
-          pblk = blk;
-          pmask = mask;
-          ++cnt;
+          sc.unit = id;
+          sc.cnt = 0;
+          // Q of the unit into L2 ahead of its TMA load
+          for (int c = 0; c < C::NCH; ++c) tma_prefetch_l2_2d(&tm_q, c * C::CH, bh * p.n + t * 128);
+          return true;
         }
-        if (!ok) break;
-        if (cnt > 0) {
-          const uint32_t info = (cnt == 1 ? kEntFirst : 0u) | kEntLast | qbuf | (pmask << 4) | ((uint32_t)pblk << 8);
-          if (!(ok = publish((uint32_t)(bh * p.n + pblk * BN), (uint32_t)id, info))) break;
-          ++uq;
+      };
+      // publish stream s's next entry; claim its next unit after the last one
+      auto step = [&](StreamCur& sc, uint32_t sflag) -> bool {
+        int32_t nblk;
+        uint32_t nmask;
+        const bool more = sc.cur.next(nblk, nmask);
+        const int bh = sc.unit / p.n_qtiles;
+        const uint32_t info = (sc.cnt == 0 ? kEntFirst : 0u) | (more ? 0u : kEntLast) | sflag | (sc.pmask << 4) |
+                              ((uint32_t)sc.pblk << 8);
+        if (!publish((uint32_t)(bh * p.n + sc.pblk * BN), (uint32_t)sc.unit, info)) return false;
+        if (more) {
+          sc.pblk = nblk;
+          sc.pmask = nmask;
+          ++sc.cnt;
+          return true;
         }
-        if (cur.bad) atomicOr(p.err, kErrBadSupport);
-        const int slot = u % URING;
-        if (u >= URING && !(ok = mbar_wait(&u_empty[slot], ((u / URING) - 1) & 1, abort_flag, p.err))) break;
-        uring[2 * slot] = id;
-        uring[2 * slot + 1] = cnt;
-        mbar_arrive(&u_full[slot]);
-        ++u;
-      }
-      if (ok) ok = publish(0u, 0u, kEntEnd);
-      if (ok) {
-        const int slot = u % URING;
-        if (u < URING || mbar_wait(&u_empty[slot], ((u / URING) - 1) & 1, abort_flag, p.err)) {
-          uring[2 * slot] = -1;
-          uring[2 * slot + 1] = 0;
-          mbar_arrive(&u_full[slot]);
-        }
+        if (sc.cur.bad) atomicOr(p.err, kErrBadSupport);
+        sc.alive = claim(sc);
+        return sc.alive || publish(0u, 0u, kEntMark | sflag);
+      };
+      sc0.alive = claim(sc0);
+      if (!sc0.alive) ok = publish(0u, 0u, kEntMark);
+      sc1.alive = ok && claim(sc1);
+      if (ok && !sc1.alive) ok = publish(0u, 0u, kEntMark | kEntStream);
+      int s = 0;
+      while (ok && (sc0.alive || sc1.alive)) {
+        if (s == 0 && !sc0.alive) s = 1;
+        else if (s == 1 && !sc1.alive) s = 0;
+        ok = s ? step(sc1, kEntStream) : step(sc0, 0u);
+        s ^= 1;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ TMA loads
-    // Q (at the first entry of each unit), K and V. K runs KLEAD entries ahead
-    // of V: entry j's K is needed for S_j, which precedes the softmax and PV_j,
-    // which need V_j. The whole warp runs the loop; one elected lane issues.
+    // Records in order; K runs up to KLEAD records ahead of V (the MMA thread
+    // needs K of a stream's next entry right after V of its current one).
+    // The whole warp runs the loop; one elected lane issues.
     const bool leader = elect_one();
-    constexpr int KLEAD = (NK - 1 < 2) ? NK - 1 : 2;
+    constexpr uint32_t KLEAD = 2;
     if (leader) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
-    uint32_t nq[2] = {0u, 0u};  // Q loads per buffer
-    uint32_t jk = 0, jv = 0;    // K and V loads issued
-    bool k_end = false, ok = true;
-    while (ok) {
-      // K for entry jk while it is at most KLEAD ahead of V
-      while (ok && !k_end && jk <= jv + KLEAD) {
-        EntryRec e;
-        ok = __all_sync(0xffffffffu, wait_entry(meta, META, jk, e, abort_flag, p.err));
-        if (!ok) break;
-        if (e.info & kEntEnd) {
-          k_end = true;
-          break;
+    uint32_t nq0 = 0u, nq1 = 0u;  // Q loads per stream
+    uint32_t rk = 0, rv = 0;    // next record for K / V
+    uint32_t nk = 0, nv = 0;    // K / V loads issued
+    int kends = 0, vends = 0;   // end markers passed
+    bool ok = true;
+    while (ok && vends < 2) {
+      const bool k_turn = kends < 2 && rk < rv + KLEAD;
+      EntryRec e;
+      ok = __all_sync(0xffffffffu, wait_entry<2, true>(meta, META, k_turn ? rk : rv, e, abort_flag, p.err));
+      if (!ok) break;
+      if (k_turn) {
+        ++rk;
+        if (e.info & kEntMark) {
+          ++kends;
+          continue;
         }
+        const int s = (e.info & kEntStream) ? 1 : 0;
         if (e.info & kEntFirst) {
-          const int qb = (e.info & kEntQbuf) ? 1 : 0;
-          // the previous unit in this buffer has finished its S MMAs
-          if (nq[qb] > 0) ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[qb], (nq[qb] - 1) & 1, abort_flag, p.err));
+          // the stream's previous unit has finished its S MMAs
+          const uint32_t nqs = s ? nq1 : nq0;
+          if (nqs > 0) ok = __all_sync(0xffffffffu, mbar_wait<2>(&q_empty[s], (nqs - 1) & 1, abort_flag, p.err));
           if (!ok) break;
           const int bh = (int)e.unit / p.n_qtiles, t = (int)e.unit % p.n_qtiles;
-          const int row = bh * p.n + t * 128;
-          uint8_t* sq = smem + C::OFF_Q + qb * C::Q_BYTES;
+          uint8_t* sq = smem + C::OFF_Q + s * C::Q_BYTES;
           if (leader) {
-            mbar_arrive_expect_tx(&q_full[qb], C::Q_BYTES);
-            for (int c = 0; c < C::NCH; ++c) tma_load_2d(sq + c * 128 * ROWB, &tm_q, &q_full[qb], c * C::CH, row);
+            mbar_arrive_expect_tx(&q_full[s], C::Q_BYTES);
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_2d(sq + c * 128 * ROWB, &tm_q, &q_full[s], c * C::CH, bh * p.n + t * 128);
           }
-          ++nq[qb];
+          if (s) ++nq1;
+          else ++nq0;
         }
-        const int s = (int)(jk % NK);
-        if (jk >= (uint32_t)NK) ok = __all_sync(0xffffffffu, mbar_wait(&k_empty[s], ((jk / NK) - 1) & 1, abort_flag, p.err));
+        const int slot = (int)(nk % NK);
+        if (nk >= (uint32_t)NK)
+          ok = __all_sync(0xffffffffu, mbar_wait<2>(&k_empty[slot], ((nk / NK) - 1) & 1, abort_flag, p.err));
         if (!ok) break;
-        uint8_t* dst = smem + C::OFF_K + s * C::KV_BYTES;
+        uint8_t* dst = smem + C::OFF_K + slot * C::KV_BYTES;
         if (leader) {
-          mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
-          for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * BN * ROWB, &tm_k, &k_full[s], c * C::CH, (int)e.krow);
+          mbar_arrive_expect_tx(&k_full[slot], C::KV_BYTES);
+          for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * BN * ROWB, &tm_k, &k_full[slot], c * C::CH, (int)e.krow);
         }
-        ++jk;
-        __syncwarp();
+        ++nk;
+      } else {
+        ++rv;
+        if (e.info & kEntMark) {
+          ++vends;
+          continue;
+        }
+        const int slot = (int)(nv % NV);
+        if (nv >= (uint32_t)NV)
+          ok = __all_sync(0xffffffffu, mbar_wait<2>(&v_empty[slot], ((nv / NV) - 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        uint8_t* dst = smem + C::OFF_V + slot * C::KV_BYTES;
+        if (leader) {
+          mbar_arrive_expect_tx(&v_full[slot], C::KV_BYTES);
+          for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * BN * ROWB, &tm_v, &v_full[slot], c * C::CH, (int)e.krow);
+        }
+        ++nv;
       }
-      if (!ok || jv == jk) break;  // jv == jk only once the entry stream has ended
-      // V for entry jv (its record is already published)
-      EntryRec e;
-      ok = __all_sync(0xffffffffu, wait_entry(meta, META, jv, e, abort_flag, p.err));
-      if (!ok) break;
-      const int s = (int)(jv % NV);
-      if (jv >= (uint32_t)NV) ok = __all_sync(0xffffffffu, mbar_wait(&v_empty[s], ((jv / NV) - 1) & 1, abort_flag, p.err));
-      if (!ok) break;
-      uint8_t* dst = smem + C::OFF_V + s * C::KV_BYTES;
-      if (leader) {
-        mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
-        for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * BN * ROWB, &tm_v, &v_full[s], c * C::CH, (int)e.krow);
-      }
-      ++jv;
       __syncwarp();
     }
     // No copy into this CTA's shared memory may outlive the CTA.
     if (leader) {
-      for (uint32_t i = (jk > (uint32_t)NK ? jk - NK : 0u); i < jk; ++i)
-        mbar_wait_drain(&k_full[i % NK], (i / NK) & 1, p.err);
-      for (uint32_t i = (jv > (uint32_t)NV ? jv - NV : 0u); i < jv; ++i)
-        mbar_wait_drain(&v_full[i % NV], (i / NV) & 1, p.err);
-      for (int qb = 0; qb < 2; ++qb)
-        if (nq[qb] > 0) mbar_wait_drain(&q_full[qb], (nq[qb] - 1) & 1, p.err);
+      for (uint32_t i = (nk > (uint32_t)NK ? nk - NK : 0u); i < nk; ++i)
+        mbar_wait_drain<2>(&k_full[i % NK], (i / NK) & 1, p.err);
+      for (uint32_t i = (nv > (uint32_t)NV ? nv - NV : 0u); i < nv; ++i)
+        mbar_wait_drain<2>(&v_full[i % NV], (i / NV) & 1, p.err);
+      if (nq0 > 0) mbar_wait_drain<2>(&q_full[0], (nq0 - 1) & 1, p.err);
+      if (nq1 > 0) mbar_wait_drain<2>(&q_full[1], (nq1 - 1) & 1, p.err);
     }
     __syncwarp();
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------------------------ MMA issuers
-    // Warp 2 issues S_j = Q K_j^T, warp 3 issues O += P_j V_j. Each whole warp
-    // runs its loop (barrier waits and descriptor arithmetic stay warp-uniform)
-    // and one elected lane issues the MMAs and their commits: single-lane
-    // issue loops lose most of their issue slots to the softmax warps sharing
-    // the SM sub-partition. Both walk the entry records in order. S_{j+NSB}
-    // reuses the TMEM buffer of P_j and is issued once PV_j has completed.
+  } else {
+    // ------------------------------------------------------------ MMA issue
+    // Warp 2 issues the MMAs of stream 0, warp 3 those of stream 1. For each
+    // record of its stream: O_s += P_s V once the softmax has written P_s,
+    // then S_s = Q_s K^T of the stream's next record, both from the same
+    // elected thread, so the S MMA executes after the PV MMA that reads P_s
+    // from the same TMEM columns. Records of the other stream are skipped but
+    // counted: K and V slots are assigned in record order. The whole warp
+    // runs the loop (waits stay warp-uniform); one elected lane issues.
+    const int s = warp - 2;
+    const uint32_t sflag = s ? kEntStream : 0u;
     const bool leader = elect_one();
-    if (warp == 2) {
-      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
-      uint32_t nq[2] = {0u, 0u};  // units per Q buffer whose S MMAs began
-      bool ok = true;
-      for (uint32_t j = 0; ok; ++j) {
-        EntryRec e;
-        ok = __all_sync(0xffffffffu, wait_entry(meta, META, j, e, abort_flag, p.err));
-        if (!ok || (e.info & kEntEnd)) break;
-        const int qb = (e.info & kEntQbuf) ? 1 : 0;
-        const int b = (int)(j % NSB);
-        if (j >= (uint32_t)NSB) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((j / NSB) - 1) & 1, abort_flag, p.err));
-        if (ok && (e.info & kEntFirst)) ok = __all_sync(0xffffffffu, mbar_wait(&q_full[qb], nq[qb] & 1, abort_flag, p.err));
-        const int s = (int)(j % NK);
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&k_full[s], (j / NK) & 1, abort_flag, p.err));
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t qd = smem_desc(smem_u32(smem + C::OFF_Q + qb * C::Q_BYTES), 16, 8 * ROWB, C::SWZ);
-        const uint64_t kd = smem_desc(smem_u32(smem + C::OFF_K + s * C::KV_BYTES), 16, 8 * ROWB, C::SWZ);
-        const uint32_t dS = tbase + C::s_col(b);
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int c = kk / (C::CH / 16), w = kk % (C::CH / 16);
-            // descriptor start addresses advance in 16-byte units
-            umma_ss(dS, qd + (uint64_t)((c * 128 * ROWB + w * 32) >> 4), kd + (uint64_t)((c * BN * ROWB + w * 32) >> 4),
-                    IDESC_S, kk > 0);
-          }
-          umma_commit(&s_full[b]);
-          umma_commit(&k_empty[s]);
-          if (e.info & kEntLast) umma_commit(&q_empty[qb]);  // the unit's last read of its Q buffer
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
+    constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
+    const uint64_t qd = smem_desc(smem_u32(smem + C::OFF_Q + s * C::Q_BYTES), 16, 8 * ROWB, C::SWZ);
+    const uint64_t kd_base = smem_desc(smem_u32(smem + C::OFF_K), 16, 8 * ROWB, C::SWZ);
+    const uint64_t vd_base = smem_desc(smem_u32(smem + C::OFF_V), BN * ROWB, 8 * ROWB, C::SWZ);
+    const uint32_t dS = tbase + C::s_col(s);
+    const uint32_t dO = tbase + C::o_col(s);
+    uint32_t* qpos = s ? qpos1 : qpos0;
+    uint32_t scan = 0u, ord = 0u;  // next record to read; K/V records read so far
+    uint32_t nqs = 0u, npv = 0u, nun = 0u;
+    bool ok = true;
+    // the stream's next record (index i, K/V ordinal o); false at its end
+    // marker or on abort (then ok is false too)
+    auto next_own = [&](EntryRec& e, uint32_t& i, uint32_t& o) -> bool {
+      for (;;) {
+        if (!__all_sync(0xffffffffu, wait_entry<3, false>(meta, META, scan, e, abort_flag, p.err))) {
+          ok = false;
+          return false;
         }
-        if (e.info & kEntLast) ++nq[qb];
-        __syncwarp();
-      }
-      if (leader) {
-        umma_commit(&drain[0]);  // every MMA of this thread done before TMEM is released
-        mbar_wait_drain(&drain[0], 0, p.err);
-      }
-    } else {
-      constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
-      uint32_t units = 0u;  // units whose PV MMAs began
-      bool ok = true;
-      for (uint32_t j = 0; ok; ++j) {
-        EntryRec e;
-        ok = __all_sync(0xffffffffu, wait_entry(meta, META, j, e, abort_flag, p.err));
-        if (!ok || (e.info & kEntEnd)) break;
-        const int b = (int)(j % NSB);
-        const int sv = (int)(j % NV);
-        const bool first = (e.info & kEntFirst) != 0u;
-        ok = __all_sync(0xffffffffu, mbar_wait(&p_full[b], (j / NSB) & 1, abort_flag, p.err));
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&v_full[sv], (j / NV) & 1, abort_flag, p.err));
-        // the epilogue has read the previous unit's O out of TMEM
-        if (ok && first && units > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_free, (units - 1) & 1, abort_flag, p.err));
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t vd = smem_desc(smem_u32(smem + C::OFF_V + sv * C::KV_BYTES), BN * ROWB, 8 * ROWB, C::SWZ);
-        const uint32_t aP = tbase + C::s_col(b);
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            umma_ts(tbase + C::O_COL, aP + kk * 8, vd + (uint64_t)((kk * 16 * ROWB) >> 4), IDESC_O,
-                    (first && kk == 0) ? 0u : 1u);
-          umma_commit(&v_empty[sv]);
-          umma_commit(&pv_done[b]);
-          if (e.info & kEntLast) umma_commit(o_final);
-          st_release_smem(pv_issued, j + 1u);
+        const uint32_t idx = scan++;
+        if (e.info & kEntMark) {
+          if ((e.info & kEntStream) == sflag) return false;
+          continue;
         }
-        if (e.info & kEntLast) ++units;
-        __syncwarp();
+        const uint32_t oo = ord++;
+        if ((e.info & kEntStream) == sflag) {
+          i = idx;
+          o = oo;
+          return true;
+        }
       }
+    };
+    // operands of S_s for the record with K/V ordinal o are in shared memory
+    auto wait_s = [&](const EntryRec& e, uint32_t o) -> bool {
+      if (e.info & kEntFirst) {
+        if (!__all_sync(0xffffffffu, mbar_wait<3>(&q_full[s], nqs & 1, abort_flag, p.err))) return false;
+        ++nqs;
+      }
+      return __all_sync(0xffffffffu, mbar_wait<3>(&k_full[o % NK], (o / NK) & 1, abort_flag, p.err));
+    };
+    // S_s = Q_s K^T for the record with K/V ordinal o (operands waited for)
+    auto issue_s = [&](const EntryRec& e, uint32_t o) {
+      const int slot = (int)(o % NK);
+      // descriptor start addresses advance in 16-byte units
+      const uint64_t kd = kd_base + (uint64_t)((slot * C::KV_BYTES) >> 4);
       if (leader) {
-        umma_commit(&drain[1]);
-        mbar_wait_drain(&drain[1], 0, p.err);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk / (C::CH / 16), w = kk % (C::CH / 16);
+          umma_ss(dS, qd + (uint64_t)((c * 128 * ROWB + w * 32) >> 4), kd + (uint64_t)((c * BN * ROWB + w * 32) >> 4),
+                  IDESC_S, kk > 0);
+        }
+        umma_commit(&s_full[s]);
+        umma_commit(&k_empty[slot]);
+        if (e.info & kEntLast) umma_commit(&q_empty[s]);  // the unit's last read of its Q buffer
+      }
+      __syncwarp();
+    };
+    // announce a completed unit (or, with end = 2, this issuer's end) to the epilogue
+    auto announce = [&](uint32_t end) {
+      const uint32_t n = atomicAdd(comp_tail, 1u);
+      comp[n % 8u] = ((n + 1u) << 2) | end | (uint32_t)s;
+      mbar_arrive(&comp_full[n % 8u]);
+    };
+    EntryRec cur;
+    uint32_t ci = 0u, co = 0u;
+    bool have = next_own(cur, ci, co);
+    if (have) {
+      ok = wait_s(cur, co);
+      if (ok) {
+        tc_fence_after();
+        issue_s(cur, co);
       }
     }
+    while (ok && have) {
+      // While the softmax works on the current record: read the next record
+      // and wait for every operand except P, so that the PV MMA and the next
+      // S MMA issue back to back once P is written.
+      EntryRec nxt;
+      uint32_t ni = 0u, no = 0u;
+      const bool have_next = next_own(nxt, ni, no);
+      if (!ok) break;
+      const bool first = (cur.info & kEntFirst) != 0u;
+      const int vslot = (int)(co % NV);
+      ok = __all_sync(0xffffffffu, mbar_wait<3>(&v_full[vslot], (co / NV) & 1, abort_flag, p.err));
+      // the epilogue has read the stream's previous O out of TMEM
+      if (ok && first && nun > 0) ok = __all_sync(0xffffffffu, mbar_wait<3>(&o_free[s], (nun - 1) & 1, abort_flag, p.err));
+      if (ok && have_next) ok = wait_s(nxt, no);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait<3>(&p_full[s], npv & 1, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t vd = vd_base + (uint64_t)((vslot * C::KV_BYTES) >> 4);
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts(dO, dS + kk * 8, vd + (uint64_t)((kk * 16 * ROWB) >> 4), IDESC_O, (first && kk == 0) ? 0u : 1u);
+        umma_commit(&v_empty[vslot]);
+        if (cur.info & kEntLast) {
+          umma_commit(&o_final[s]);
+          announce(0u);
+        }
+        *reinterpret_cast<volatile uint32_t*>(qpos) = ci + 1u;
+      }
+      ++npv;
+      if (first) ++nun;
+      __syncwarp();
+      if (have_next) issue_s(nxt, no);
+      cur = nxt;
+      ci = ni;
+      co = no;
+      have = have_next;
+    }
+    if (leader) {
+      *reinterpret_cast<volatile uint32_t*>(qpos) = 0x7fffffffu;  // no longer holds back the scheduler
+      announce(2u);  // also after an abort: the epilogue stops at both ends
+      umma_commit(&drain[s]);  // every MMA of this thread done before TMEM is released
+      mbar_wait_drain<3>(&drain[s], 0, p.err);
+    }
     __syncwarp();
+  }
   } else if (warp < 12) {
+    setmaxnreg_inc<184>();
     // ------------------------------------------------------------ softmax
-    const int h = (warp - 4) >> 2;       // which half of the key columns
+    const int s = (warp - 4) >> 2;  // stream
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;   // row within the query tile = TMEM lane
+    const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
     const uint32_t trow = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = trow + C::s_col(s);
+    const uint32_t tO = trow + C::o_col(s);
     const float sl2 = p.scale_log2;
     const bool want_mass = (!SPARSE) && (p.mass != nullptr);
     const int half = (BN == 64) ? (r >> 6) : 0;
-    constexpr int NC = C::HB / 32;       // 32-column chunks per half row
-    constexpr int DH = D / 2;            // O columns this warpgroup rescales
+    constexpr int NC = BN / 32;  // 32-column chunks of a score row
+    float* st = stats + s * C::ST_STRIDE;
     float m_ref = -INFINITY, l = 0.f, lt = 0.f;
-    uint32_t cnt = 0, su = 0;
+    uint32_t cnt = 0, ne = 0, nst = 0;
     int t = 0, bh = 0;
     float* lam = nullptr;
-    for (uint32_t j = 0;; ++j) {
+    for (uint32_t rec = 0;; ++rec) {
       EntryRec e;
-      bool ok = wait_entry(meta, META, j, e, abort_flag, p.err);
-      ok = __all_sync(0xffffffffu, ok);
-      // every thread reads the same record; the end is taken after the
-      // exchange barrier below so that all 256 threads leave together
-      const bool end = ok && (e.info & kEntEnd);
-      const int b = (int)(j % NSB);
-      if (ok && !end) ok = mbar_wait(&s_full[b], (j / NSB) & 1, abort_flag, p.err);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok && !end && (e.info & kEntFirst)) {
+      bool ok = __all_sync(0xffffffffu, wait_entry<4, false>(meta, META, rec, e, abort_flag, p.err));
+      if (!ok) break;
+      if ((((e.info & kEntStream) != 0u) ? 1 : 0) != s) continue;
+      if (e.info & kEntMark) break;
+      ok = __all_sync(0xffffffffu, mbar_wait<4>(&s_full[s], ne & 1, abort_flag, p.err));
+      if (!ok) break;
+      if (e.info & kEntFirst) {
+        e.unit = meta[rec % (uint32_t)META].unit;  // ordered after the tag's acquire load
         bh = (int)e.unit / p.n_qtiles;
         t = (int)e.unit % p.n_qtiles;
         m_ref = -INFINITY;
         l = 0.f;
         lt = 0.f;
         cnt = 0;
-        lam = want_mass ? p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + h * 128 + r : nullptr;
+        lam = want_mass ? p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + r : nullptr;
       }
-      const uint32_t tS = trow + C::s_col(b);
-      uint32_t s[NC][32];
-      float mxh = -INFINITY;
-      int limit = -1;
-      if (ok && !end) {
-        tc_fence_after();
+      tc_fence_after();
+      uint32_t v[NC][32];
 #pragma unroll
-        for (int cc = 0; cc < NC; ++cc) tmem_ld_x32(tS + h * C::HB + cc * 32, s[cc]);
+      for (int cc = 0; cc < NC; ++cc) tmem_ld_x32(tS + cc * 32, v[cc]);
 #pragma unroll
-        for (int cc = 0; cc < NC; ++cc) tmem_wait_ld(s[cc]);
-        const int kbase = (int)(e.info >> 8) * BN;
-        const int qpos = t * 128 + r;
-        const bool row_on = (e.info >> (4 + half)) & 1u;
-        // columns c <= limit of the tile are admissible (causal mask M, working-set mask R)
-        limit = row_on ? ((kbase + BN - 1 > qpos) ? qpos - kbase : BN) : -1;
-        if (limit < h * C::HB + C::HB - 1) {
-#pragma unroll
-          for (int cc = 0; cc < NC; ++cc)
-#pragma unroll
-            for (int q = 0; q < 32; ++q)
-              s[cc][q] = (h * C::HB + cc * 32 + q <= limit) ? s[cc][q] : __float_as_uint(-INFINITY);
-        }
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      for (int cc = 0; cc < NC; ++cc) tmem_wait_ld(v[cc]);
+      const int kbase = (int)(e.info >> 8) * BN;
+      const int qpos = t * 128 + r;
+      const bool row_on = (e.info >> (4 + half)) & 1u;
+      // columns c <= limit of the tile are admissible (causal mask M, working-set mask R)
+      const int limit = row_on ? ((kbase + BN - 1 > qpos) ? qpos - kbase : BN) : -1;
+      if (limit < BN - 1) {
 #pragma unroll
         for (int cc = 0; cc < NC; ++cc)
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            mx4[q & 3] = fmax3(mx4[q & 3], __uint_as_float(s[cc][2 * q]), __uint_as_float(s[cc][2 * q + 1]));
-        mxh = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
-      } else if (lane == 0) {
-        atomicMin(sm_abort, (int)j);
+          for (int q = 0; q < 32; ++q) v[cc][q] = (cc * 32 + q <= limit) ? v[cc][q] : __float_as_uint(-INFINITY);
       }
-      // both halves' loads of S are complete before either writes P over it
-      tc_fence_before();
-      xch[(j & 1) * 256 + h * 128 + r] = mxh;
-      named_bar_sync(1, 256);
-      if (end || *reinterpret_cast<volatile int*>(sm_abort) <= (int)j) break;
-      tc_fence_after();
-      const float mx = fmaxf(mxh, xch[(j & 1) * 256 + (1 - h) * 128 + r]) * sl2;
+      // row max: eight independent 3-input max chains
+      float mx8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < NC; ++cc)
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          mx8[q & 7] = fmax3(mx8[q & 7], __uint_as_float(v[cc][2 * q]), __uint_as_float(v[cc][2 * q + 1]));
+      const float mx =
+          fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
       float factor = 1.f;
       bool resc = false;
       if (cnt == 0) {
@@ -690,7 +794,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           float e0, e1;
-          f2_unpack(ffma2(f2_pack(__uint_as_float(s[cc][2 * q]), __uint_as_float(s[cc][2 * q + 1])), sc2, nm2), e0,
+          f2_unpack(ffma2(f2_pack(__uint_as_float(v[cc][2 * q]), __uint_as_float(v[cc][2 * q + 1])), sc2, nm2), e0,
                     e1);
           const float p0 = fast_exp2(e0);
           const float p1 = fast_exp2(e1);
@@ -698,7 +802,7 @@ __global__ void __launch_bounds__(512, 1)
           rs2[q & 1] = fadd2(rs2[q & 1], f2_pack(p0, p1));
           add_bf16x2_to(rt2[q & 1], pk[q]);
         }
-        tmem_st_x16(tS + h * (C::HB / 2) + cc * 16, pk);
+        tmem_st_x16(tS + cc * 16, pk);
       }
       float rs, rt;
       {
@@ -710,115 +814,105 @@ __global__ void __launch_bounds__(512, 1)
       }
       l = l * factor + rs;
       lt = lt * factor + rt;
-      if (__any_sync(0xffffffffu, resc)) {
-        // O of this unit holds PV up to entry j-1: wait for the last one
-        const uint32_t jb = j - 1u;
-        bool okw = mbar_wait(&pv_done[jb % NSB], (jb / NSB) & 1, abort_flag, p.err);
-        okw = __all_sync(0xffffffffu, okw);
-        if (okw) {
-          tc_fence_after();
-          rescale_o(trow + C::O_COL + h * DH, DH, factor);
-        } else if (lane == 0) {
-          atomicMin(sm_abort, (int)j + 1);
-        }
-      }
+      // O_s holds every PV MMA up to the previous entry (the S_s commit
+      // covers them); rows whose max jumped are rescaled in place
+      if (__any_sync(0xffffffffu, resc)) rescale_o(tO, D, factor);
       tmem_wait_st();
-      if (want_mass) lam[(size_t)cnt * 256] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
+      if (want_mass) lam[(size_t)cnt * 128] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[b]);
+      if (lane == 0) mbar_arrive(&p_full[s]);
+      ++ne;
       ++cnt;
       if (e.info & kEntLast) {
-        // per-row statistics of the unit for the epilogue
-        const int sb = (int)(su & 1);
-        bool okw = (su < 2) || mbar_wait(&st_empty[sb], ((su >> 1) - 1) & 1, abort_flag, p.err);
-        okw = __all_sync(0xffffffffu, okw);
-        if (okw) {
-          float* st = stats + sb * 5 * 128;
-          if (h == 0) st[r] = m_ref;
-          st[(1 + h) * 128 + r] = l;
-          st[(3 + h) * 128 + r] = lt;
+        // per-row results of the unit for the epilogue
+        ok = (nst == 0) || __all_sync(0xffffffffu, mbar_wait<4>(&st_empty[s], (nst - 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        st[r] = (l > 0.f) ? m_use + fast_log2(l) : -INFINITY;
+        st[128 + r] = (lt > 0.f) ? 1.f / lt : 0.f;
+        if (quarter == 0 && lane == 0) {
+          reinterpret_cast<int*>(st)[256] = bh * p.n_qtiles + t;
+          reinterpret_cast<int*>(st)[257] = (int)cnt;
         }
         __syncwarp();
-        if (lane == 0) {
-          if (okw) mbar_arrive(&st_full[sb]);
-          else atomicMin(sm_abort, (int)j + 1);
-        }
-        ++su;
+        if (lane == 0) mbar_arrive(&st_full[s]);
+        ++nst;
       }
     }
   } else {
+    setmaxnreg_dec<64>();
     // ------------------------------------------------------------ epilogue
+    // Serves the units of both streams in the order the MMA thread issued
+    // their last PV MMA (the order in which their O accumulators complete).
+    // All four warps walk the same completion list; named barrier 2 keeps
+    // them together around the shared statistics and the mass partials.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const uint32_t tO = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + C::O_COL;
     const bool want_mass = (!SPARSE) && (p.mass != nullptr);
-    uint32_t eu = 0;  // units with entries processed (o_final / stats phases)
-    for (int u = 0;; ++u) {
-      const int slot = u % URING;
-      bool ok = mbar_wait(&u_full[slot], (u / URING) & 1, abort_flag, p.err);
-      ok = __all_sync(0xffffffffu, ok);
-      int id = -1, cnt = 0;
-      if (ok) {
-        id = uring[2 * slot];
-        cnt = uring[2 * slot + 1];
+    uint32_t served0 = 0u, served1 = 0u;  // units served per stream
+    int ends = 0;
+    for (uint32_t n = 0;; ++n) {
+      // next completed unit: its completion word is published through an
+      // mbarrier (the waiting threads sleep instead of polling shared memory)
+      bool ok = __all_sync(0xffffffffu, mbar_wait<5>(&comp_full[n % 8u], (n / 8u) & 1u, abort_flag, p.err));
+      const uint32_t w = ok ? comp[n % 8u] : 0u;
+      if (ok && (w >> 2) != n + 1u) {  // overrun, which the O hand-off rules out
+        *abort_flag = 1;
+        atomicOr(p.err, kErrTimeout);
+        ok = false;
       }
-      __syncwarp();
-      if (ok && lane == 0) mbar_arrive(&u_empty[slot]);
-      const bool end = ok && id < 0;  // every epilogue thread reads the same record
-      if (end) cnt = 0;
-      const int bh = ok ? id / p.n_qtiles : 0, t = ok ? id % p.n_qtiles : 0;
+      ok = __all_sync(0xffffffffu, ok);
+      const bool end = ok && (w & 2u);
+      const int s = (int)(w & 1u);
+      float* st = stats + s * C::ST_STRIDE;
+      int id = -1, cnt = 0;
+      float lse2 = 0.f, inv_l = 0.f;
+      const uint32_t served = s ? served1 : served0;
+      if (ok && !end) {
+        ok = __all_sync(0xffffffffu, mbar_wait<5>(&st_full[s], served & 1, abort_flag, p.err));
+        if (ok) {
+          id = reinterpret_cast<const int*>(st)[256];
+          cnt = reinterpret_cast<const int*>(st)[257];
+          lse2 = st[r];
+          inv_l = st[128 + r];
+          ok = __all_sync(0xffffffffu, mbar_wait<5>(&o_final[s], served & 1, abort_flag, p.err));
+        }
+      }
+      if (!ok && lane == 0) atomicOr(ep_bad, 1);
+      named_bar_sync(2, 128);  // every warp has read the statistics
+      if (*reinterpret_cast<volatile int*>(ep_bad)) break;
+      if (end) {
+        if (++ends == 2) break;  // both issuers have finished
+        continue;
+      }
+      const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
       const int qpos = t * 128 + r;
       const bool row_valid = qpos < p.n;
       const size_t grow = (size_t)bh * p.n + qpos;
-      float m = 0.f, lsum = 0.f, ltsum = 0.f;
-      if (ok && cnt > 0) {
-        const int sb = (int)(eu & 1);
-        ok = mbar_wait(&st_full[sb], (eu >> 1) & 1, abort_flag, p.err);
-        if (ok) {
-          const float* st = stats + sb * 5 * 128;
-          m = st[r];
-          lsum = st[128 + r] + st[256 + r];
-          ltsum = st[384 + r] + st[512 + r];
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        __syncwarp();
-        if (ok && lane == 0) mbar_arrive(&st_empty[sb]);
-        if (ok) ok = mbar_wait(o_final, eu & 1, abort_flag, p.err);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (!ok && lane == 0) atomicMin(ep_abort, u);
-      named_bar_sync(2, 128);
-      if (end || *reinterpret_cast<volatile int*>(ep_abort) <= u) break;
-      const float inv_l = (ltsum > 0.f) ? 1.f / ltsum : 0.f;
-      if (cnt > 0) tc_fence_after();
+      const uint32_t tO = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + C::o_col(s);
+      tc_fence_after();
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        if (cnt > 0) {
-          tmem_ld_x32(tO + cc * 32, o);
-          tmem_wait_ld(o);
-          if (cc == D / 32 - 1) {
-            // O is out of TMEM: the next unit's PV may overwrite it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_free);
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] = 0u;
+      for (int cc = 0; cc < D / 16; ++cc) {
+        uint32_t o[16];
+        tmem_ld_x16(tO + cc * 16, o);
+        tmem_wait_ld16(o);
+        if (cc == D / 16 - 1) {
+          // O is out of TMEM: the stream's next PV may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_free[s]);
         }
         if (row_valid) {
           if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + grow * D + cc * 32);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + grow * D + cc * 16);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < 4; ++q)
               dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
                                    __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D + cc * 32);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D + cc * 16);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
               uint4 v;
               v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
               v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
@@ -829,19 +923,18 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
-      const float lse2 = (lsum > 0.f) ? m + fast_log2(lsum) : -INFINITY;
       if (p.lse != nullptr && row_valid) p.lse[grow] = lse2 * 0.69314718055994531f;
       if (want_mass) {
-        // Eq 5: r_qb = (1/B) * sum over the block's rows of 2^(lam_ib - lse2_i),
-        // lam summed over the two column halves. Entries go through `part`
-        // 64 at a time; blocks past the unit's entries are zero.
+        // Eq 5: r_qb = (1/B) * sum over the block's rows of 2^(lam_ib - lse2_i).
+        // Partial sums per warp go through the stream's statistics area (read
+        // above), 64 entries at a time; blocks past the unit's entries are zero.
+        float* part = st;
         const float* lam = p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + r;
+        const bool row_has = row_valid && lse2 > -INFINITY;
         for (int c0 = 0; c0 < cnt; c0 += 64) {
           const int c1 = min(cnt, c0 + 64);
           for (int e = c0; e < c1; ++e) {
-            float a = 0.f;
-            if (row_valid && lsum > 0.f)
-              a = fast_exp2(lam[(size_t)e * 256] - lse2) + fast_exp2(lam[(size_t)e * 256 + 128] - lse2);
+            float a = row_has ? fast_exp2(lam[(size_t)e * 128] - lse2) : 0.f;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
             if (lane == 0) part[quarter * 64 + (e - c0)] = a;
@@ -872,7 +965,10 @@ __global__ void __launch_bounds__(512, 1)
           for (int e = cnt + r; e < p.nb; e += 128) dst[e] = 0.f;
         }
       }
-      if (cnt > 0) ++eu;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st_empty[s]);
+      if (s) ++served1;
+      else ++served0;
     }
   }
 
@@ -882,15 +978,7 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
-  if (threadIdx.x == 0) {
-    // every CTA has pulled its last position: the last one out resets the slot
-    __threadfence();
-    if (atomicAdd(&g_sched[p.sched_slot].done, 1u) == gridDim.x - 1) {
-      g_sched[p.sched_slot].next = 0u;
-      g_sched[p.sched_slot].done = 0u;
-      __threadfence();
-    }
-  }
+  if (threadIdx.x == 0) sched_slot_done(p);
 }
 
 }  // namespace wise

@@ -8,7 +8,7 @@
 namespace wise {
 
 // Bits of the device error word.
-enum : uint32_t { kErrBadSupport = 1u, kErrTimeout = 2u };
+enum : uint32_t { kErrBadSupport = 1u, kErrTimeout = 2u, kErrInternal = 4u };
 
 // Every mbarrier wait in this library gives up after this long and reports
 // WISE_ERR_DEVICE_TIMEOUT instead of hanging the GPU.
@@ -52,8 +52,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Slow path of mbar_wait, kept out of line so that the many call sites in the
 // hot loops stay small (the kernels' code competes for instruction cache).
+// TAG gives each warp role of a kernel its own out-of-line copy: a function
+// called from regions with different setmaxnreg register counts cannot be
+// register-allocated.
+template <int TAG>
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                             uint32_t* err_word) {
   const uint64_t t0 = global_timer_ns();
@@ -73,10 +90,11 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 // Wait for the phase of `bar` with the given parity. Gives up (returns false)
 // when another role of the CTA has aborted or after kWaitLimitNs, in which
 // case it raises the abort flag and records kErrTimeout.
+template <int TAG = 0>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err_word) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, err_word);
+  return mbar_wait_slow<TAG>(bar, parity, abort_flag, err_word);
 }
 
 // ----------------------------------------------------------------------- TMA
@@ -90,6 +108,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "[%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+
+// Asynchronous prefetch of one tensor tile into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // ------------------------------------------------------------------- tcgen05
@@ -297,6 +322,11 @@ __device__ __forceinline__ bool elect_one() {
 __device__ __forceinline__ uint32_t ld_acquire_smem(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_acquire_smem_b64(const void* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.cta.shared::cta.b64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_release_smem(uint32_t* p, uint32_t v) {

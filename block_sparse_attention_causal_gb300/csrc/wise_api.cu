@@ -118,7 +118,7 @@ Shape shape_of(const wise_attn_desc* d) {
 size_t lam_bytes(const Shape& s) {
   const int64_t ept = 128 / s.bn;
   const int64_t per_bh = ept * (int64_t)s.n_qtiles * (s.n_qtiles + 1) / 2;
-  return (size_t)(s.bh * per_bh * 256 * sizeof(float));
+  return (size_t)(s.bh * per_bh * 128 * sizeof(float));
 }
 
 int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -382,6 +382,7 @@ int wise_device_status(wise_stream_t stream) {
   if (cudaMemcpyFromSymbol(&word, g_wise_error_word, sizeof(word)) != cudaSuccess) return WISE_ERR_CUDA;
   if (word && cudaMemcpyToSymbol(g_wise_error_word, &zero, sizeof(zero)) != cudaSuccess) return WISE_ERR_CUDA;
   if (word & kErrTimeout) return WISE_ERR_DEVICE_TIMEOUT;
+  if (word & kErrInternal) return WISE_ERR_CUDA;
   if (word & kErrBadSupport) return WISE_ERR_BAD_SUPPORT;
   return WISE_OK;
 }

@@ -44,9 +44,9 @@ def test_workspace_and_capacity_queries(lib):
     assert lib.wise_support_capacity(d) == 2 * nb * (nb + 1) // 2
     # one 128-row query tile per unit; n = 256 -> two units per (batch, head)
     assert lib.wise_schedule_units(d) == 4
-    # lambda scratch: (128/B) * T(T+1)/2 entries of 2 x 128 floats (two column
-    # halves) per (b,h), T = 2 query tiles
-    assert lib.wise_attn_discover_workspace(d) == 2 * (2 * 3) * 256 * 4
+    # lambda scratch: (128/B) * T(T+1)/2 entries of 128 floats (one per row)
+    # per (b,h), T = 2 query tiles
+    assert lib.wise_attn_discover_workspace(d) == 2 * (2 * 3) * 128 * 4
     assert lib.wise_select_workspace(d, 2) > 0
     assert lib.wise_select_workspace(d, 0) == 0
     assert lib.wise_schedule_units(_desc(1, 1, 128 * 5, 128, 128)) == 5

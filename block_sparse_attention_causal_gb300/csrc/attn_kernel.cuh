@@ -396,11 +396,16 @@ __global__ void __launch_bounds__(512, 1)
       SchedSlot* sched = &g_sched[p.sched_slot];
       uint32_t j = 0;  // records published
       bool ok = true;
-      // Publish one record once the flow control allows slot j. qpos_s is one
-      // past the last record whose PV MMA stream s's issuer has issued; every
-      // reader (softmax, loader, issuers) is at or beyond min(qpos0, qpos1),
-      // and four slots of the ring stay out of the scheduler's reach.
-      constexpr uint32_t AHEAD = (uint32_t)META - 4u;
+      // Publish record j once j < min(qpos0, qpos1) + AHEAD, where qpos_s is
+      // one past the last record whose PV MMA stream s's issuer has issued.
+      // Every reader (softmax, loader, issuers) is at or beyond that minimum,
+      // so the ring is never overrun. AHEAD is also the claim horizon: units
+      // are taken from the shared work counter only a few records before
+      // they are needed, which keeps the CTAs' finishing times close. It
+      // must exceed the issuers' read-ahead (their next record can be three
+      // records past the minimum's stream position plus one marker).
+      constexpr uint32_t AHEAD = 10u;
+      static_assert(AHEAD + 4u <= (uint32_t)META, "record ring");
       auto publish = [&](uint32_t krow, uint32_t unit, uint32_t info) -> bool {
         if (j >= AHEAD) {
           const uint64_t t0 = global_timer_ns();
@@ -511,7 +516,10 @@ __global__ void __launch_bounds__(512, 1)
     int kends = 0, vends = 0;   // end markers passed
     bool ok = true;
     while (ok && vends < 2) {
-      const bool k_turn = kends < 2 && rk < rv + KLEAD;
+      // K only if its record is already published: V (of an earlier record)
+      // must never wait behind an unpublished record
+      const bool k_turn = kends < 2 && rk < rv + KLEAD &&
+                          (rk == rv || ld_acquire_smem(&meta[rk % (uint32_t)META].tag) == rk + 1u);
       EntryRec e;
       ok = __all_sync(0xffffffffu, wait_entry<2, true>(meta, META, k_turn ? rk : rv, e, abort_flag, p.err));
       if (!ok) break;

@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(512, 1)
   int* ep_bad = reinterpret_cast<int*>(misc + 3);
   uint32_t* qpos1 = misc + 4;
   uint32_t* comp_tail = misc + 5;
+  uint32_t* marks_seen = misc + 6;  // [2] softmax warps of stream s past its end marker
   // completed units in the order their last PV MMA was issued: word n % 8 =
   // (n + 1) << 2 | end flag << 1 | stream, announced on comp_full[n % 8]
   uint32_t* comp = misc + 8;
@@ -373,6 +374,8 @@ __global__ void __launch_bounds__(512, 1)
     *qpos0 = 0u;
     *qpos1 = 0u;
     *comp_tail = 0u;
+    marks_seen[0] = 0u;
+    marks_seen[1] = 0u;
     *ep_bad = 0;
     for (int i = 0; i < 8; ++i) comp[i] = 0u;
     fence_mbar_init();
@@ -397,9 +400,11 @@ __global__ void __launch_bounds__(512, 1)
       uint32_t j = 0;  // records published
       bool ok = true;
       // Publish record j once j < min(qpos0, qpos1) + AHEAD, where qpos_s is
-      // one past the last record whose PV MMA stream s's issuer has issued.
-      // Every reader (softmax, loader, issuers) is at or beyond that minimum,
-      // so the ring is never overrun. AHEAD is also the claim horizon: units
+      // one past the last record whose PV MMA stream s's issuer has issued,
+      // raised to "no limit" only once all four softmax warps of stream s
+      // have read its end marker (they scan the records up to it after the
+      // issuer has finished). Every reader (softmax, loader, issuers) is at
+      // or beyond that minimum, so the ring is never overrun. AHEAD is also the claim horizon: units
       // are taken from the shared work counter only a few records before
       // they are needed, which keeps the CTAs' finishing times close. It
       // must exceed the issuers' read-ahead (their next record can be three
@@ -697,7 +702,7 @@ __global__ void __launch_bounds__(512, 1)
           umma_commit(&o_final[s]);
           announce(0u);
         }
-        *reinterpret_cast<volatile uint32_t*>(qpos) = ci + 1u;
+        atomicMax(qpos, ci + 1u);
       }
       ++npv;
       if (first) ++nun;
@@ -709,7 +714,6 @@ __global__ void __launch_bounds__(512, 1)
       have = have_next;
     }
     if (leader) {
-      *reinterpret_cast<volatile uint32_t*>(qpos) = 0x7fffffffu;  // no longer holds back the scheduler
       announce(2u);  // also after an abort: the epilogue stops at both ends
       umma_commit(&drain[s]);  // every MMA of this thread done before TMEM is released
       mbar_wait_drain<3>(&drain[s], 0, p.err);
@@ -739,7 +743,12 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = __all_sync(0xffffffffu, wait_entry<4, false>(meta, META, rec, e, abort_flag, p.err));
       if (!ok) break;
       if ((((e.info & kEntStream) != 0u) ? 1 : 0) != s) continue;
-      if (e.info & kEntMark) break;
+      if (e.info & kEntMark) {
+        // the last of the stream's softmax warps to get here releases the
+        // stream's hold on the scheduler
+        if (lane == 0 && atomicAdd(&marks_seen[s], 1u) == 3u) atomicMax(s ? qpos1 : qpos0, 0x7fffffffu);
+        break;
+      }
       ok = __all_sync(0xffffffffu, mbar_wait<4>(&s_full[s], ne & 1, abort_flag, p.err));
       if (!ok) break;
       if (e.info & kEntFirst) {

@@ -245,10 +245,30 @@ def identification_margin(r_q: Sequence[float], q: int, eta: float) -> float:
     return max(0.0, min(terms))
 
 
+def retained_mass_rows(r: np.ndarray, rows: Sequence[Sequence[int]]) -> np.ndarray:
+    """Retained future attention mass per query block (WISE App. B,
+    "Evaluation metrics"): sum over the support's key blocks of the
+    unrestricted block masses r_qb (Eq 5) of a later step."""
+    return np.array([sum(float(r[q, b]) for b in rows[q]) for q in range(len(rows))], np.float64)
+
+
 def retained_mass(r: np.ndarray, rows: Sequence[Sequence[int]]) -> float:
     """Mean over query blocks of sum_{b in B_q} r_qb: the share of the
     unrestricted attention mass that lands inside the support."""
-    return float(np.mean([sum(r[q, b] for b in rows[q]) for q in range(len(rows))]))
+    return float(np.mean(retained_mass_rows(r, rows)))
+
+
+def jaccard(rows_a: Sequence[Sequence[int]], rows_b: Sequence[Sequence[int]]) -> Tuple[int, int, float]:
+    """WISE App. C.2 Eq 24 for one example: the working sets are the
+    collections of active (head, query block, key block) entries; returns
+    (|A intersect B|, |A union B|, their ratio), the ratio being 1 when both are empty.
+    rows_a and rows_b list the key blocks of the same sequence of rows."""
+    inter = union = 0
+    for ra, rb in zip(rows_a, rows_b):
+        sa, sb = set(ra), set(rb)
+        inter += len(sa & sb)
+        union += len(sa | sb)
+    return inter, union, (inter / union if union else 1.0)
 
 
 # ---------------------------------------------------------------------------

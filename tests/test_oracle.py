@@ -288,3 +288,41 @@ def test_retained_mass_and_density():
     rows = [[0], [0, 1], [2]]
     assert abs(W.retained_mass(r, rows) - (1.0 + 1.0 + 0.7) / 3) < 1e-15
     assert abs(W.block_density(rows) - 4 / 6) < 1e-15
+
+
+# ------------------------------------------ App. B retained mass, App. C.2 Eq 24 ----
+
+def test_retained_mass_rows_full_support_keeps_all_mass():
+    """The full causal support keeps every row's whole mass (Eq 5 rows sum to
+    one); the diagonal-only support keeps exactly r_qq."""
+    q, k, _ = _rand(256, 32, seed=11, scale=2.0)
+    r = W.block_mass(q, k, 64)
+    nb = r.shape[0]
+    full = W.retained_mass_rows(r, [list(range(qb + 1)) for qb in range(nb)])
+    assert np.all(np.abs(full - 1.0) < 1e-12)
+    diag = W.retained_mass_rows(r, [[qb] for qb in range(nb)])
+    assert np.array_equal(diag, np.diag(r))
+
+
+def test_jaccard_hand_example():
+    """Rows {0}|{0}, {0,1}|{1}, {0,2}|{1,2}: intersections 1+1+1, unions 1+2+3."""
+    inter, union, j = W.jaccard([[0], [0, 1], [0, 2]], [[0], [1], [1, 2]])
+    assert (inter, union) == (3, 6) and j == 0.5
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_jaccard_against_boolean_matrices(seed):
+    """Eq 24 through boolean (row, key block) incidence matrices; plus the
+    invariants J(A, A) = 1, symmetry and |A and B| + |A or B| = |A| + |B|."""
+    rng = np.random.default_rng(seed)
+    rows, nb = 40, 24
+    a = rng.random((rows, nb)) < 0.3
+    b = rng.random((rows, nb)) < 0.4
+    la = [np.nonzero(x)[0].tolist() for x in a]
+    lb = [np.nonzero(x)[0].tolist() for x in b]
+    inter, union, j = W.jaccard(la, lb)
+    assert inter == int(np.sum(a & b)) and union == int(np.sum(a | b))
+    assert inter + union == int(a.sum() + b.sum())
+    assert W.jaccard(lb, la) == (inter, union, j)
+    assert W.jaccard(la, la)[2] == 1.0
+    assert W.jaccard([[] for _ in range(rows)], [[] for _ in range(rows)]) == (0, 0, 1.0)

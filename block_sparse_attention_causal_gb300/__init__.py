@@ -27,7 +27,8 @@ from . import _lib
 from ._lib import (WISE_BF16, WISE_F32, WISE_SUPPORT_DIAG, WISE_SUPPORT_SINK, WiseError)  # noqa: F401
 
 __all__ = ["discover", "select_support", "sparse", "Support", "device_status", "WiseError",
-           "WISE_SUPPORT_SINK", "WISE_SUPPORT_DIAG", "useful_flops", "dense_flops"]
+           "WISE_SUPPORT_SINK", "WISE_SUPPORT_DIAG", "useful_flops", "dense_flops", "retained_mass",
+           "support_jaccard"]
 
 _OUT = {torch.bfloat16: WISE_BF16, torch.float32: WISE_F32}
 
@@ -191,6 +192,48 @@ def support_from_lists(rows, batch: int, heads: int, seq_len: int, head_dim: int
                    torch.zeros(max(units, 1), dtype=torch.int32, device=device),
                    torch.tensor([len(cols)], dtype=torch.int32, device=device),
                    batch, heads, seq_len, head_dim, block)
+
+
+def retained_mass(masses: torch.Tensor, support: Support, *, stream: Optional[torch.cuda.Stream] = None):
+    """Retained future attention mass (WISE App. B metrics) of a support for a
+    later step's block masses [B, H, nb, nb] (f32, from :func:`discover`).
+    Returns (per-row fractions [B*H*nb] f32, per-batch mean [B] f64)."""
+    if not masses.is_cuda or masses.dtype != torch.float32 or masses.dim() != 4 or not masses.is_contiguous():
+        raise ValueError("masses must be a contiguous float32 CUDA tensor [B, H, nb, nb]")
+    b, h, nb, _ = masses.shape
+    if (b, h, nb) != (support.batch, support.heads, support.n_blocks):
+        raise ValueError("masses do not match the support's shape")
+    lib = _lib.load()
+    desc = _lib.make_desc(support.batch, support.heads, support.seq_len, support.head_dim, support.block)
+    rows = torch.empty(b * h * nb, dtype=torch.float32, device=masses.device)
+    mean = torch.empty(b, dtype=torch.float64, device=masses.device)
+    st = lib.wise_support_retained_mass(desc, masses.data_ptr(), support.row_ptr.data_ptr(),
+                                        support.col_idx.data_ptr(), support.col_idx.numel(), rows.data_ptr(),
+                                        mean.data_ptr(), _stream_handle(stream))
+    _lib.check(st, "wise_support_retained_mass")
+    return rows, mean
+
+
+def support_jaccard(a: Support, b: Support, *, stream: Optional[torch.cuda.Stream] = None):
+    """Rolling working-set stability (WISE App. C.2 Eq 24) between two
+    supports of the same shape. Returns (per-row counts [B*H*nb, 2] int32 of
+    |A and B|, |A or B|; per-batch summed counts [B, 2] int64; per-batch
+    Jaccard index [B] f64)."""
+    shape = (a.batch, a.heads, a.seq_len, a.head_dim, a.block)
+    if shape != (b.batch, b.heads, b.seq_len, b.head_dim, b.block):
+        raise ValueError("supports of different shapes")
+    lib = _lib.load()
+    desc = _lib.make_desc(*shape)
+    rows = a.batch * a.heads * a.n_blocks
+    dev = a.row_ptr.device
+    row_counts = torch.empty((rows, 2), dtype=torch.int32, device=dev)
+    counts = torch.empty((a.batch, 2), dtype=torch.int64, device=dev)
+    jac = torch.empty(a.batch, dtype=torch.float64, device=dev)
+    st = lib.wise_support_jaccard(desc, a.row_ptr.data_ptr(), a.col_idx.data_ptr(), a.col_idx.numel(),
+                                  b.row_ptr.data_ptr(), b.col_idx.data_ptr(), b.col_idx.numel(),
+                                  row_counts.data_ptr(), counts.data_ptr(), jac.data_ptr(), _stream_handle(stream))
+    _lib.check(st, "wise_support_jaccard")
+    return row_counts, counts, jac
 
 
 def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -31,6 +31,7 @@ EXPORTS = (
     "wise_abi_version", "wise_status_str", "wise_attn_discover_workspace", "wise_attn_discover",
     "wise_schedule_units", "wise_support_capacity", "wise_select_workspace", "wise_select_support",
     "wise_attn_sparse", "wise_validate_support", "wise_device_status", "wise_select_support_noalloc",
+    "wise_support_retained_mass", "wise_support_jaccard",
 )
 
 
@@ -76,6 +77,8 @@ _SIGNATURES = {
                                                    _vp, _vp]),
     "wise_attn_sparse": (ctypes.c_int, [_dp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "wise_validate_support": (ctypes.c_int, [_dp, _vp, _vp, _u32]),
+    "wise_support_retained_mass": (ctypes.c_int, [_dp, _vp, _vp, _vp, _i64, _vp, _vp, _vp]),
+    "wise_support_jaccard": (ctypes.c_int, [_dp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "wise_device_status": (ctypes.c_int, [_vp]),
 }
 

@@ -51,4 +51,25 @@ cudaError_t launch_attn_d128(int block, bool sparse, const CUtensorMap* maps, co
 
 cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream);
 
+// Support diagnostics (diag_kernel.cu): retained future attention mass and
+// the Jaccard index of two supports.
+struct DiagLaunch {
+  int64_t rows;  // batch * heads * nb CSR rows
+  int32_t nb, batch;
+  int64_t col_cap;           // col_idx entries of support A that may be read
+  int64_t col_cap_b;         // ... of support B
+  const float* mass;         // [rows, nb] (retained mass)
+  const int32_t* row_ptr_a;  // support A (the only one for retained mass)
+  const int32_t* col_idx_a;
+  const int32_t* row_ptr_b;  // support B (Jaccard)
+  const int32_t* col_idx_b;
+  float* row_value;          // [rows] retained mass per row
+  int32_t* row_counts;       // [rows][2] |A intersect B|, |A union B| per row
+  double* batch_value;       // [batch] mean retained mass or Jaccard index (optional)
+  long long* batch_counts;   // [batch][2] summed counts (optional)
+  uint32_t* err;
+};
+cudaError_t launch_retained_mass(const DiagLaunch& d, cudaStream_t stream);
+cudaError_t launch_jaccard(const DiagLaunch& d, cudaStream_t stream);
+
 }  // namespace wise

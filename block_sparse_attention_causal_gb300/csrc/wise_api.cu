@@ -350,6 +350,69 @@ int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_m
   return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
 }
 
+int wise_support_retained_mass(const wise_attn_desc* desc, const float* block_mass, const int32_t* row_ptr,
+                                const int32_t* col_idx, int64_t col_capacity, float* row_retained, double* batch_mean,
+                                wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!block_mass || !row_ptr || !col_idx || !row_retained || col_capacity < 0) return WISE_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(block_mass) & 3u) || (reinterpret_cast<uintptr_t>(row_ptr) & 3u) ||
+      (reinterpret_cast<uintptr_t>(col_idx) & 3u) || (reinterpret_cast<uintptr_t>(row_retained) & 3u) ||
+      (batch_mean && (reinterpret_cast<uintptr_t>(batch_mean) & 7u)))
+    return WISE_ERR_ALIGNMENT;
+  uint32_t* err = error_word();
+  if (!err) return WISE_ERR_CUDA;
+  const Shape s = shape_of(desc);
+  DiagLaunch d;
+  memset(&d, 0, sizeof(d));
+  d.rows = s.bh * s.nb;
+  d.nb = s.nb;
+  d.batch = desc->batch;
+  d.col_cap = col_capacity;
+  d.mass = block_mass;
+  d.row_ptr_a = row_ptr;
+  d.col_idx_a = col_idx;
+  d.row_value = row_retained;
+  d.batch_value = batch_mean;
+  d.err = err;
+  return launch_retained_mass(d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
+}
+
+int wise_support_jaccard(const wise_attn_desc* desc, const int32_t* row_ptr_a, const int32_t* col_idx_a,
+                         int64_t col_capacity_a, const int32_t* row_ptr_b, const int32_t* col_idx_b,
+                         int64_t col_capacity_b, int32_t* row_counts, int64_t* batch_counts, double* batch_jaccard,
+                         wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!row_ptr_a || !col_idx_a || !row_ptr_b || !col_idx_b || !row_counts || col_capacity_a < 0 ||
+      col_capacity_b < 0)
+    return WISE_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(row_ptr_a) & 3u) || (reinterpret_cast<uintptr_t>(col_idx_a) & 3u) ||
+      (reinterpret_cast<uintptr_t>(row_ptr_b) & 3u) || (reinterpret_cast<uintptr_t>(col_idx_b) & 3u) ||
+      (reinterpret_cast<uintptr_t>(row_counts) & 3u) || (batch_counts && (reinterpret_cast<uintptr_t>(batch_counts) & 7u)) ||
+      (batch_jaccard && (reinterpret_cast<uintptr_t>(batch_jaccard) & 7u)))
+    return WISE_ERR_ALIGNMENT;
+  uint32_t* err = error_word();
+  if (!err) return WISE_ERR_CUDA;
+  const Shape s = shape_of(desc);
+  DiagLaunch d;
+  memset(&d, 0, sizeof(d));
+  d.rows = s.bh * s.nb;
+  d.nb = s.nb;
+  d.batch = desc->batch;
+  d.col_cap = col_capacity_a;
+  d.col_cap_b = col_capacity_b;
+  d.row_ptr_a = row_ptr_a;
+  d.col_idx_a = col_idx_a;
+  d.row_ptr_b = row_ptr_b;
+  d.col_idx_b = col_idx_b;
+  d.row_counts = row_counts;
+  d.batch_counts = reinterpret_cast<long long*>(batch_counts);
+  d.batch_value = batch_jaccard;
+  d.err = err;
+  return launch_jaccard(d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
+}
+
 int wise_validate_support(const wise_attn_desc* desc, const int32_t* row_ptr, const int32_t* col_idx,
                           uint32_t flags) {
   int st = check_desc(desc);

@@ -15,7 +15,11 @@
  *                        built once after discovery);
  *   wise_attn_sparse     §5.2 Eqs 7-8 (late-step attention restricted to the
  *                        reused support; Q/K/V and the within-support softmax
- *                        are recomputed on every call).
+ *                        are recomputed on every call);
+ *   wise_support_retained_mass, wise_support_jaccard
+ *                        the support diagnostics of Appendix B ("retained
+ *                        future attention mass") and Appendix C.2 Eq 24
+ *                        (rolling working-set Jaccard stability).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -202,6 +206,46 @@ int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_m
 int wise_attn_sparse(const wise_attn_desc* desc, const void* q, const void* k, const void* v,
                      const int32_t* row_ptr, const int32_t* col_idx, int64_t col_capacity,
                      const int32_t* tile_order, void* o, float* lse, wise_stream_t stream);
+
+/*
+ * wise_support_retained_mass -- retained future attention mass (WISE
+ * Appendix B, "Evaluation metrics"): the fraction of a later step's
+ * unrestricted attention mass that falls inside a (frozen) support.
+ *   block_mass   : [batch, heads, nb, nb] float32 block masses r_qb of the
+ *                  later step, as wise_attn_discover writes them (device).
+ *   row_ptr, col_idx, col_capacity : the support CSR (device), as for
+ *                  wise_attn_sparse.
+ *   row_retained : [batch * heads * nb] float32 (device, caller-owned):
+ *                  sum over the row's listed key blocks b <= q of r_qb.
+ *   batch_mean   : [batch] float64 (device, optional): mean of row_retained
+ *                  over the heads x nb rows of each batch element.
+ * Entries outside 0 <= b <= q are skipped and flagged (WISE_ERR_BAD_SUPPORT).
+ * The row sums are accumulated in float64 in a fixed order, so repeated calls
+ * give identical results.
+ */
+int wise_support_retained_mass(const wise_attn_desc* desc, const float* block_mass, const int32_t* row_ptr,
+                                const int32_t* col_idx, int64_t col_capacity, float* row_retained,
+                                double* batch_mean, wise_stream_t stream);
+
+/*
+ * wise_support_jaccard -- rolling working-set stability (WISE Appendix C.2
+ * Eq 24): the Jaccard index of two supports A and B over all active
+ * (head, query block, key block) entries of each batch element.
+ *   row_ptr_a, col_idx_a, col_capacity_a, row_ptr_b, col_idx_b,
+ *   col_capacity_b : two support CSRs of the same shape (device), each with
+ *                  the number of col_idx entries that may be read.
+ *   row_counts   : [batch * heads * nb][2] int32 (device, caller-owned):
+ *                  |A_q intersect B_q| and |A_q union B_q| per row.
+ *   batch_counts : [batch][2] int64 (device, optional): their sums.
+ *   batch_jaccard: [batch] float64 (device, optional): sum of intersections
+ *                  / sum of unions (1 when both supports are empty).
+ * Sets, not lists, are compared: repeated entries count once; entries outside
+ * 0 <= b <= q are skipped and flagged (WISE_ERR_BAD_SUPPORT).
+ */
+int wise_support_jaccard(const wise_attn_desc* desc, const int32_t* row_ptr_a, const int32_t* col_idx_a,
+                         int64_t col_capacity_a, const int32_t* row_ptr_b, const int32_t* col_idx_b,
+                         int64_t col_capacity_b, int32_t* row_counts, int64_t* batch_counts, double* batch_jaccard,
+                         wise_stream_t stream);
 
 /* Host-side check of a support CSR (host pointers): row_ptr monotone from 0,
  * every row strictly ascending with 0 <= b <= q, and, if the flags ask for

@@ -355,12 +355,42 @@ def run_gpu(args, rank, world):
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_traj_ms, 3)},
         "gpu_launches": launches,
     }
+    result["support_quality"] = support_quality(wise, cfg, dev_in, support, masses, ws, o, lse)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows_all = support.to_lists()
         by_head = [((b_, h_), rows_all[(b_ * H + h_) * nb:(b_ * H + h_ + 1) * nb])
                    for b_ in range(B) for h_ in range(H)]
         result["cpu_baseline"] = cpu_baseline(cfg, seed, by_head)
     return result
+
+
+def support_quality(wise, cfg, dev_in, frozen, masses, ws, o, lse):
+    """WISE's own support diagnostics on this workload, outside the timed
+    region: block masses of unrestricted attention at every step, the rolling
+    working sets W(t) (union of the step supports of steps max(0, t-3)..t,
+    App. C.2 Eq 23), their adjacent Jaccard index (Eq 24) at the discovery
+    depth, the drift J(W(t_d - 1), W(T - 1)), and the retained future
+    attention mass of the frozen support at each late step (App. B)."""
+    import torch
+    B, H, n, d, blk = cfg.batch, cfg.heads, cfg.seq_len, cfg.head_dim, cfg.block
+    step_mass = []
+    for t in range(cfg.steps):
+        m = torch.empty_like(masses[0])
+        wise.discover(dev_in[t][0], dev_in[t][1], dev_in[t][2], blk, out=o, lse=lse, mass=m, workspace=ws)
+        step_mass.append(m)
+    rolling = [wise.select_support(torch.stack(step_mass[max(0, t - 3):t + 1]).contiguous(), n, d, blk, cfg.eta)
+               for t in range(cfg.steps)]
+    td = cfg.t_d
+    adj = [float(wise.support_jaccard(rolling[t - 1], rolling[t])[2].mean().item()) for t in range(1, cfg.steps)]
+    retained = [float(wise.retained_mass(step_mass[t], frozen)[1].mean().item()) for t in range(td, cfg.steps)]
+    drift = float(wise.support_jaccard(rolling[td - 1], rolling[cfg.steps - 1])[2].mean().item())
+    wise.check_device()
+    return {"retained_future_mass": {"mean": round(sum(retained) / len(retained), 5),
+                                     "per_late_step": [round(x, 5) for x in retained]},
+            "rolling_jaccard_adjacent": [round(x, 5) for x in adj],
+            "rolling_jaccard_at_td": round(adj[td - 2], 5) if td >= 2 else None,
+            "drift_jaccard_td_to_T": round(drift, 5),
+            "definitions": "retained mass: App. B; rolling sets: Eq 23 (0-indexed steps); Jaccard: Eq 24"}
 
 
 # --------------------------------------------------------------------------- oracle (CPU) arm

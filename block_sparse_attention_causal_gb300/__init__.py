@@ -42,7 +42,9 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> None:
+def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
+    """Validates the operands; returns the number of key/value heads (fewer
+    than the query heads for grouped-query attention)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
@@ -50,15 +52,18 @@ def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> None:
             raise ValueError(f"{name} must be bfloat16")
         if not t.is_contiguous() or t.dim() != 4:
             raise ValueError(f"{name} must be a contiguous [batch, heads, seq, head_dim] tensor")
-    if q.shape != k.shape or q.shape != v.shape:
-        raise ValueError("q, k, v must have the same shape")
+    b, h, n, d = q.shape
+    hk = k.shape[1]
+    if k.shape != v.shape or k.shape != (b, hk, n, d) or hk < 1 or h % hk != 0:
+        raise ValueError("k and v must be [batch, kv_heads, seq, head_dim] with kv_heads dividing q's heads")
+    return hk
 
 
-def _desc(shape: Sequence[int], block: int, scale: float, out_dtype: torch.dtype) -> _lib.AttnDesc:
+def _desc(shape: Sequence[int], block: int, scale: float, out_dtype: torch.dtype, kv_heads: int = 0) -> _lib.AttnDesc:
     b, h, n, d = shape
     if out_dtype not in _OUT:
         raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
-    return _lib.make_desc(b, h, n, d, block, scale, _OUT[out_dtype])
+    return _lib.make_desc(b, h, n, d, block, scale, _OUT[out_dtype], kv_heads)
 
 
 def discover_workspace_bytes(shape: Sequence[int], block: int) -> int:
@@ -71,11 +76,12 @@ def discover(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: int, *, w
              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
              mass: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None):
-    """Discovery step. Returns (O, LSE or None, block masses [B,H,nb,nb] or None)."""
-    _check_qkv(q, k, v)
+    """Discovery step. Returns (O, LSE or None, block masses [B,H,nb,nb] or None).
+    k and v may have fewer heads than q (grouped-query attention)."""
+    hk = _check_qkv(q, k, v)
     lib = _lib.load()
     b, h, n, d = q.shape
-    desc = _desc(q.shape, block, scale, out_dtype)
+    desc = _desc(q.shape, block, scale, out_dtype, hk)
     if out is None:
         out = torch.empty((b, h, n, d), dtype=out_dtype, device=q.device)
     if want_lse and lse is None:
@@ -103,7 +109,7 @@ class Support:
     """The reused working set: CSR over rows (batch, head, query block)."""
     row_ptr: torch.Tensor      # int32 [B*H*nb + 1]
     col_idx: torch.Tensor      # int32 [capacity]
-    tile_order: torch.Tensor   # int32 [units]: late-step work order
+    tile_order: Optional[torch.Tensor]  # int32 [units]: late-step work order (None: natural order)
     nnz: torch.Tensor          # int32 [1] (device)
     batch: int
     heads: int
@@ -156,20 +162,22 @@ def sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, support: Support, 
            out_dtype: torch.dtype = torch.bfloat16, scale: float = 0.0, out: Optional[torch.Tensor] = None,
            lse: Optional[torch.Tensor] = None, use_schedule: bool = True,
            stream: Optional[torch.cuda.Stream] = None):
-    """Late (reuse) step over the support. Returns (O, LSE or None)."""
-    _check_qkv(q, k, v)
+    """Late (reuse) step over the support. Returns (O, LSE or None).
+    k and v may have fewer heads than q (grouped-query attention)."""
+    hk = _check_qkv(q, k, v)
     lib = _lib.load()
     b, h, n, d = q.shape
     if (b, h, n, d) != (support.batch, support.heads, support.seq_len, support.head_dim):
         raise ValueError("support was built for a different shape")
-    desc = _desc(q.shape, support.block, scale, out_dtype)
+    desc = _desc(q.shape, support.block, scale, out_dtype, hk)
     if out is None:
         out = torch.empty((b, h, n, d), dtype=out_dtype, device=q.device)
     if want_lse and lse is None:
         lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
     st = lib.wise_attn_sparse(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), support.row_ptr.data_ptr(),
                               support.col_idx.data_ptr(), support.col_idx.numel(),
-                              support.tile_order.data_ptr() if use_schedule else None, out.data_ptr(),
+                              support.tile_order.data_ptr() if (use_schedule and support.tile_order is not None)
+                              else None, out.data_ptr(),
                               _ptr(lse) if want_lse else None, _stream_handle(stream))
     _lib.check(st, "wise_attn_sparse")
     return out, (lse if want_lse else None)
@@ -178,18 +186,16 @@ def sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, support: Support, 
 def support_from_lists(rows, batch: int, heads: int, seq_len: int, head_dim: int, block: int,
                        device="cuda") -> Support:
     """A Support from explicit ascending key-block lists (rows ordered batch,
-    head, query block); tile_order is left to the kernel's natural order."""
-    lib = _lib.load()
+    head, query block). It has no work order: late steps over it use the
+    kernel's natural order."""
     rp = [0]
     cols = []
     for r in rows:
         cols.extend(int(x) for x in r)
         rp.append(len(cols))
-    desc = _lib.make_desc(batch, heads, seq_len, head_dim, block)
-    units = int(lib.wise_schedule_units(desc))
     return Support(torch.tensor(rp, dtype=torch.int32, device=device),
                    torch.tensor(cols if cols else [0], dtype=torch.int32, device=device),
-                   torch.zeros(max(units, 1), dtype=torch.int32, device=device),
+                   None,
                    torch.tensor([len(cols)], dtype=torch.int32, device=device),
                    batch, heads, seq_len, head_dim, block)
 

@@ -50,6 +50,7 @@ class AttnDesc(ctypes.Structure):
         ("block", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
         ("out_dtype", ctypes.c_int32),
+        ("kv_heads", ctypes.c_int32),
     ]
 
 
@@ -121,5 +122,5 @@ def check(status: int, what: str = "") -> None:
 
 
 def make_desc(batch: int, heads: int, seq_len: int, head_dim: int, block: int, scale: float = 0.0,
-              out_dtype: int = WISE_BF16) -> AttnDesc:
-    return AttnDesc(batch, heads, seq_len, head_dim, block, scale, out_dtype)
+              out_dtype: int = WISE_BF16, kv_heads: int = 0) -> AttnDesc:
+    return AttnDesc(batch, heads, seq_len, head_dim, block, scale, out_dtype, kv_heads)

@@ -204,7 +204,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 struct __align__(16) EntryRec {
   uint32_t tag;
   uint32_t info;   // flags | block index << 8
-  uint32_t krow;   // global row of the key block's first key (TMA coordinate)
+  uint32_t krow;   // global row of the key block's first key in K/V (TMA coordinate)
   uint32_t unit;   // unit id = bh * n_qtiles + tile
 };
 
@@ -439,6 +439,7 @@ __global__ void __launch_bounds__(512, 1)
       struct StreamCur {
         TileCursor cur;
         int unit, cnt;
+        uint32_t kvrow0;  // first K/V row of the unit's key/value head
         int32_t pblk;
         uint32_t pmask;
         bool alive;
@@ -466,6 +467,8 @@ __global__ void __launch_bounds__(512, 1)
           }
           sc.unit = id;
           sc.cnt = 0;
+          // the key/value head of query head bh (grouped-query attention)
+          sc.kvrow0 = (uint32_t)(((bh / p.heads) * (p.heads / p.kv_group) + (bh % p.heads) / p.kv_group) * p.n);
           // Q of the unit into L2 ahead of its TMA load
           for (int c = 0; c < C::NCH; ++c) tma_prefetch_l2_2d(&tm_q, c * C::CH, bh * p.n + t * 128);
           return true;
@@ -476,10 +479,9 @@ __global__ void __launch_bounds__(512, 1)
         int32_t nblk;
         uint32_t nmask;
         const bool more = sc.cur.next(nblk, nmask);
-        const int bh = sc.unit / p.n_qtiles;
         const uint32_t info = (sc.cnt == 0 ? kEntFirst : 0u) | (more ? 0u : kEntLast) | sflag | (sc.pmask << 4) |
                               ((uint32_t)sc.pblk << 8);
-        if (!publish((uint32_t)(bh * p.n + sc.pblk * BN), (uint32_t)sc.unit, info)) return false;
+        if (!publish(sc.kvrow0 + (uint32_t)(sc.pblk * BN), (uint32_t)sc.unit, info)) return false;
         if (more) {
           sc.pblk = nblk;
           sc.pmask = nmask;

@@ -8,6 +8,8 @@ namespace wise {
 
 struct AttnParams {
   int32_t bh_count;     // batch * heads
+  int32_t heads;        // query heads per batch element
+  int32_t kv_group;     // query heads per key/value head (1 without grouped-query attention)
   int32_t n;            // sequence length
   int32_t nb;           // n / BN key (and query) blocks
   int32_t n_qtiles;     // ceil(n / 128): work units (query tiles) per (batch, head)

@@ -81,6 +81,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_desc(const wise_attn_desc* d) {
   if (!d) return WISE_ERR_INVALID_ARGUMENT;
   if (d->batch < 1 || d->heads < 1 || d->seq_len < 1 || d->block < 1) return WISE_ERR_INVALID_ARGUMENT;
+  if (d->kv_heads < 0 || (d->kv_heads > 0 && d->heads % d->kv_heads != 0)) return WISE_ERR_INVALID_ARGUMENT;
   if (d->out_dtype != WISE_BF16 && d->out_dtype != WISE_F32) return WISE_ERR_INVALID_ARGUMENT;
   if (!(d->softmax_scale >= 0.f) || isinf(d->softmax_scale)) return WISE_ERR_INVALID_ARGUMENT;
   if (d->seq_len % d->block != 0) return WISE_ERR_INVALID_ARGUMENT;
@@ -95,6 +96,7 @@ int check_desc(const wise_attn_desc* d) {
 struct Shape {
   int64_t bh;
   int n, d, bn, nb, n_qtiles, group_heads;
+  int heads, kv_heads;  // kv_heads divides heads (grouped-query attention)
   int64_t n_units;
 };
 
@@ -106,8 +108,11 @@ Shape shape_of(const wise_attn_desc* d) {
   s.bn = d->block;
   s.nb = d->seq_len / d->block;
   s.n_qtiles = (d->seq_len + 127) / 128;
-  const size_t kv_per_head = (size_t)2 * d->seq_len * d->head_dim * 2;
-  int64_t g = (int64_t)(kL2GroupBytes / kv_per_head);
+  s.heads = d->heads;
+  s.kv_heads = d->kv_heads > 0 ? d->kv_heads : d->heads;
+  // K/V bytes per query head (query heads that share a key/value head share it)
+  const size_t kv_per_head = (size_t)2 * d->seq_len * d->head_dim * 2 * s.kv_heads / s.heads;
+  int64_t g = (int64_t)(kL2GroupBytes / (kv_per_head > 0 ? kv_per_head : 1));
   if (g < 1) g = 1;
   if (g > s.bh) g = s.bh;
   s.group_heads = (int)g;
@@ -129,13 +134,16 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
   if (!err) return WISE_ERR_CUDA;
   CUtensorMap maps[3];
   const int64_t rows = s.bh * s.n;
+  const int64_t kv_rows = (int64_t)desc->batch * s.kv_heads * s.n;
   int st = encode_map(&maps[0], q, rows, s.d, 128);
-  if (st == WISE_OK) st = encode_map(&maps[1], k, rows, s.d, s.bn);
-  if (st == WISE_OK) st = encode_map(&maps[2], v, rows, s.d, s.bn);
+  if (st == WISE_OK) st = encode_map(&maps[1], k, kv_rows, s.d, s.bn);
+  if (st == WISE_OK) st = encode_map(&maps[2], v, kv_rows, s.d, s.bn);
   if (st != WISE_OK) return st;
   AttnParams p;
   memset(&p, 0, sizeof(p));
   p.bh_count = (int32_t)s.bh;
+  p.heads = s.heads;
+  p.kv_group = s.heads / s.kv_heads;
   p.n = s.n;
   p.nb = s.nb;
   p.n_qtiles = s.n_qtiles;

@@ -24,7 +24,9 @@
  * Conventions shared by every call
  * --------------------------------
  * - Tensors are dense, row-major, in device memory owned by the caller:
- *     Q, K, V, O : [batch, heads, seq_len, head_dim], head_dim contiguous;
+ *     Q, O       : [batch, heads, seq_len, head_dim], head_dim contiguous;
+ *     K, V       : [batch, kv_heads, seq_len, head_dim] (kv_heads = heads
+ *                  unless the descriptor asks for grouped-query attention);
  *     LSE        : [batch, heads, seq_len] float32, natural-log
  *                  log-sum-exp of the scaled scores of each query row;
  *     block mass : [batch, heads, nb, nb] float32, nb = seq_len / block,
@@ -32,7 +34,7 @@
  *   Q, K, V are bf16. O is bf16 or float32 (wise_attn_desc.out_dtype).
  * - Masking is causal: key j is admissible for query i iff j <= i; key block
  *   b is admissible for query block q iff b <= q. One call is one attention
- *   layer with as many key/value heads as query heads.
+ *   layer.
  * - Supported shapes: head_dim in {64, 96, 128}; block in {64, 128};
  *   seq_len a positive multiple of block with seq_len / block <= 1024;
  *   batch * heads >= 1. Base pointers of Q/K/V/O must be 16-byte aligned.
@@ -54,7 +56,7 @@
 extern "C" {
 #endif
 
-#define WISE_ABI_VERSION 1
+#define WISE_ABI_VERSION 2
 
 typedef struct CUstream_st* wise_stream_t; /* same type as cudaStream_t */
 
@@ -83,6 +85,11 @@ typedef struct wise_attn_desc {
   int32_t block;         /* B, the support block size (query and key blocks) */
   float softmax_scale;   /* 0 => 1/sqrt(head_dim), the scale of Eq 2 */
   int32_t out_dtype;     /* wise_dtype of O */
+  int32_t kv_heads;      /* key/value heads; 0 => heads. Grouped-query
+                          * attention when kv_heads < heads: kv_heads must
+                          * divide heads, and query head h reads key/value
+                          * head h / (heads / kv_heads). Masses and supports
+                          * stay per query head. */
 } wise_attn_desc;
 
 /* ABI version (WISE_ABI_VERSION) and a static string for a status code. */

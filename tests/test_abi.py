@@ -25,7 +25,20 @@ def test_header_declares_exactly_the_binding_exports():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert lib.wise_abi_version() == 1
+    version = int(re.search(r"#define WISE_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert lib.wise_abi_version() == version
+
+
+def test_grouped_query_heads_are_validated(lib):
+    """kv_heads must be 0 (= heads) or divide heads; the argument check
+    runs before any launch, so no device is needed."""
+    dummy = ctypes.c_void_p(16)
+    for kv, ok in ((0, True), (1, True), (2, True), (4, True), (3, False), (-1, False), (8, False)):
+        d = _lib.make_desc(1, 4, 256, 64, 64, 0.0, 0, kv)
+        assert (lib.wise_attn_discover_workspace(d) > 0) == ok, kv
+        if not ok:
+            st = lib.wise_attn_discover(d, dummy, dummy, dummy, dummy, None, None, None, 0, None)
+            assert st == _lib.WISE_ERR_INVALID_ARGUMENT
 
 
 def test_status_strings(lib):

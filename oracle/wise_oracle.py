@@ -183,6 +183,71 @@ def step_support(r_q: Sequence[float], q: int, eta: float,
     return kept | set(near[:k - len(kept)])
 
 
+def _cut_support(fx: Sequence[int], q: int, k: int, tie_tolerance: float) -> Set[int]:
+    """The k highest-mass admissible blocks (b <= q) in (mass desc, index asc)
+    order, with the near-tie rule of step_support at the cut."""
+    admissible = list(range(q + 1))
+    if k <= 0:
+        return set()
+    if k >= len(admissible):
+        return set(admissible)
+    order = sorted(admissible, key=lambda b: (-fx[b], b))
+    r_star = fx[order[k - 1]]
+    tol = int(to_fixed(tie_tolerance))
+    kept = {b for b in admissible if fx[b] > r_star + tol}
+    near = sorted(b for b in admissible if abs(fx[b] - r_star) <= tol)
+    return kept | set(near[:k - len(kept)])
+
+
+def mass_matched_support(r_q: Sequence[float], q: int, reference: Iterable[int],
+                         tie_tolerance: float = TIE_TOLERANCE) -> Set[int]:
+    """MassMatched control (WISE App. B "Intervention controls", Eqs 20-21):
+    the smallest set of highest-mass admissible blocks of this step whose
+    cumulative mass reaches m_q, the mass of this step covered by the
+    reference working set. m_q is summed in the same fixed point as Eq 6, so
+    the cut compares exact integers."""
+    fx = [int(x) for x in to_fixed(np.asarray(r_q, np.float64)[:q + 1])]
+    target = sum(fx[b] for b in set(reference) if 0 <= b <= q)
+    if target <= 0:
+        return set()
+    order = sorted(range(q + 1), key=lambda b: (-fx[b], b))
+    cum = 0
+    for pos, b in enumerate(order):
+        cum += fx[b]
+        if cum >= target:
+            return _cut_support(fx, q, pos + 1, tie_tolerance)
+    return set(range(q + 1))
+
+
+def size_matched_support(r_q: Sequence[float], q: int, size: int,
+                         tie_tolerance: float = TIE_TOLERANCE) -> Set[int]:
+    """SizeMatched control (WISE App. B "Intervention controls", Eq 22): the
+    `size` highest-mass admissible blocks of this step (TopK), with the near-tie
+    rule of Eq 6 (reading R6) at the cut."""
+    fx = [int(x) for x in to_fixed(np.asarray(r_q, np.float64)[:q + 1])]
+    return _cut_support(fx, q, size, tie_tolerance)
+
+
+def control_set(r: np.ndarray, reference: Sequence[Sequence[int]], mode: str,
+                flags: int = 0, tie_tolerance: float = TIE_TOLERANCE) -> List[List[int]]:
+    """MassMatched ("mass") or SizeMatched ("size") rows for one step's
+    [nb, nb] masses against the reference working set's rows; the sink and
+    diagonal blocks are added as in working_set when flags ask for them."""
+    out = []
+    for q in range(r.shape[0]):
+        ref = [b for b in reference[q] if 0 <= b <= q]
+        if mode == "mass":
+            s = mass_matched_support(r[q], q, ref, tie_tolerance)
+        else:
+            s = size_matched_support(r[q], q, len(set(ref)), tie_tolerance)
+        if flags & SUPPORT_SINK:
+            s.add(0)
+        if flags & SUPPORT_DIAG:
+            s.add(q)
+        out.append(sorted(s))
+    return out
+
+
 def working_set(masses: Sequence[np.ndarray], eta: float, flags: int = SUPPORT_SINK | SUPPORT_DIAG,
                 tie_tolerance: float = TIE_TOLERANCE) -> List[List[int]]:
     """Eq 6 (left): B_q = union over the window steps of the step supports.

@@ -326,3 +326,52 @@ def test_jaccard_against_boolean_matrices(seed):
     assert W.jaccard(lb, la) == (inter, union, j)
     assert W.jaccard(la, la)[2] == 1.0
     assert W.jaccard([[] for _ in range(rows)], [[] for _ in range(rows)]) == (0, 0, 1.0)
+
+
+# ----------------------------------------- App. B controls, Eqs 19-22 ----
+
+def test_mass_matched_hand_example():
+    """Masses (0.5, 0.3, 0.2) for q = 2; reference {1, 2} covers 0.5, which
+    the single largest block already reaches: MassMatched = {0}. Reference {2}
+    covers 0.2: again {0}. Reference {0, 1} covers 0.8: {0, 1}."""
+    r = [0.5, 0.3, 0.2]
+    assert W.mass_matched_support(r, 2, [1, 2]) == {0}
+    assert W.mass_matched_support(r, 2, [2]) == {0}
+    assert W.mass_matched_support(r, 2, [0, 1]) == {0, 1}
+    assert W.mass_matched_support(r, 2, []) == set()
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_mass_matched_is_the_smallest_set_reaching_the_reference_mass(seed):
+    """Brute force over every subset of a small row: the control has the
+    minimum cardinality among sets whose mass reaches the reference's, it
+    never has more blocks than the reference, and it reaches that mass."""
+    rng = np.random.default_rng(seed)
+    q = 6
+    r = rng.dirichlet(np.ones(q + 1))
+    ref = sorted(rng.choice(q + 1, size=3, replace=False).tolist())
+    m = sum(r[b] for b in ref)
+    got = W.mass_matched_support(r, q, ref)
+    best = min(len(c) for k in range(q + 2) for c in itertools.combinations(range(q + 1), k)
+               if sum(r[b] for b in c) >= m - 1e-12)
+    assert len(got) == best <= len(ref)
+    assert sum(r[b] for b in got) >= m - 1e-12
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_size_matched_is_numpy_top_k(seed):
+    """Eq 22 against numpy's stable sort on (-mass, index) for distinct masses."""
+    rng = np.random.default_rng(seed)
+    q = 20
+    r = rng.random(q + 1)
+    for k in (0, 1, 5, q + 1, q + 5):
+        want = set(np.lexsort((np.arange(q + 1), -r))[:k].tolist())
+        assert W.size_matched_support(r, q, k) == want
+
+
+def test_controls_with_ties_prefer_lower_indices():
+    r = [0.25, 0.25, 0.25, 0.25]
+    assert W.size_matched_support(r, 3, 2) == {0, 1}
+    assert W.mass_matched_support(r, 3, [2, 3]) == {0, 1}
+    rows = W.control_set(np.array([r] * 4), [[0], [0, 1], [1, 2], [2, 3]], "size", flags=W.SUPPORT_DIAG)
+    assert rows == [[0], [0, 1], [0, 1, 2], [0, 1, 3]]

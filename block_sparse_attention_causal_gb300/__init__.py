@@ -28,7 +28,7 @@ from ._lib import (WISE_BF16, WISE_F32, WISE_SUPPORT_DIAG, WISE_SUPPORT_SINK, Wi
 
 __all__ = ["discover", "select_support", "sparse", "Support", "device_status", "WiseError",
            "WISE_SUPPORT_SINK", "WISE_SUPPORT_DIAG", "useful_flops", "dense_flops", "retained_mass",
-           "support_jaccard"]
+           "support_jaccard", "select_control"]
 
 _OUT = {torch.bfloat16: WISE_BF16, torch.float32: WISE_F32}
 
@@ -198,6 +198,40 @@ def support_from_lists(rows, batch: int, heads: int, seq_len: int, head_dim: int
                    None,
                    torch.tensor([len(cols)], dtype=torch.int32, device=device),
                    batch, heads, seq_len, head_dim, block)
+
+
+def select_control(masses: torch.Tensor, reference: Support, mode: str, flags: int = 0, *,
+                   stream: Optional[torch.cuda.Stream] = None) -> Support:
+    """Early-static controls of WISE App. B from one step's masses [B, H, nb, nb]
+    (f32) and a reference working set: mode "mass" = MassMatched (Eqs 20-21),
+    "size" = SizeMatched (Eq 22). Static-95 (Eq 19) is select_support with a
+    window of one step and eta = 0.95."""
+    modes = {"mass": _lib.WISE_CONTROL_MASS_MATCHED, "size": _lib.WISE_CONTROL_SIZE_MATCHED}
+    if mode not in modes:
+        raise ValueError('mode must be "mass" or "size"')
+    if not masses.is_cuda or masses.dtype != torch.float32 or masses.dim() != 4 or not masses.is_contiguous():
+        raise ValueError("masses must be a contiguous float32 CUDA tensor [B, H, nb, nb]")
+    b, h, nb, _ = masses.shape
+    if (b, h, nb) != (reference.batch, reference.heads, reference.n_blocks):
+        raise ValueError("masses do not match the reference support's shape")
+    lib = _lib.load()
+    desc = _lib.make_desc(reference.batch, reference.heads, reference.seq_len, reference.head_dim, reference.block)
+    cap = int(lib.wise_support_capacity(desc))
+    units = int(lib.wise_schedule_units(desc))
+    dev = masses.device
+    out = Support(torch.empty(b * h * nb + 1, dtype=torch.int32, device=dev),
+                  torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+                  torch.empty(max(units, 1), dtype=torch.int32, device=dev),
+                  torch.empty(1, dtype=torch.int32, device=dev), reference.batch, reference.heads,
+                  reference.seq_len, reference.head_dim, reference.block)
+    ws = torch.empty(max(int(lib.wise_select_workspace(desc, 1)), 16), dtype=torch.uint8, device=dev)
+    st = lib.wise_select_control(desc, masses.data_ptr(), modes[mode], reference.row_ptr.data_ptr(),
+                                 reference.col_idx.data_ptr(), reference.col_idx.numel(), flags,
+                                 out.row_ptr.data_ptr(), out.col_idx.data_ptr(), out.col_idx.numel(),
+                                 out.tile_order.data_ptr(), out.nnz.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 _stream_handle(stream))
+    _lib.check(st, "wise_select_control")
+    return out
 
 
 def retained_mass(masses: torch.Tensor, support: Support, *, stream: Optional[torch.cuda.Stream] = None):

@@ -25,13 +25,15 @@ WISE_BF16 = 0
 WISE_F32 = 1
 WISE_SUPPORT_SINK = 1
 WISE_SUPPORT_DIAG = 2
+WISE_CONTROL_MASS_MATCHED = 1
+WISE_CONTROL_SIZE_MATCHED = 2
 
 # Every symbol include/wise.h declares.
 EXPORTS = (
     "wise_abi_version", "wise_status_str", "wise_attn_discover_workspace", "wise_attn_discover",
     "wise_schedule_units", "wise_support_capacity", "wise_select_workspace", "wise_select_support",
     "wise_attn_sparse", "wise_validate_support", "wise_device_status", "wise_select_support_noalloc",
-    "wise_support_retained_mass", "wise_support_jaccard",
+    "wise_support_retained_mass", "wise_support_jaccard", "wise_select_control",
 )
 
 
@@ -78,6 +80,8 @@ _SIGNATURES = {
                                                    _vp, _vp]),
     "wise_attn_sparse": (ctypes.c_int, [_dp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "wise_validate_support": (ctypes.c_int, [_dp, _vp, _vp, _u32]),
+    "wise_select_control": (ctypes.c_int, [_dp, _vp, _i32, _vp, _vp, _i64, _u32, _vp, _vp, _i64, _vp, _vp, _vp,
+                                           _sz, _vp]),
     "wise_support_retained_mass": (ctypes.c_int, [_dp, _vp, _vp, _vp, _i64, _vp, _vp, _vp]),
     "wise_support_jaccard": (ctypes.c_int, [_dp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "wise_device_status": (ctypes.c_int, [_vp]),

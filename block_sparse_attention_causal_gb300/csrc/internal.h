@@ -42,6 +42,10 @@ struct SelectLaunch {
   int32_t* nnz;
   int32_t* tile_order;
   int32_t units_per_bh, qb_per_unit, group_heads;
+  int32_t mode;                // 0: Eq 6; 1: MassMatched; 2: SizeMatched (window 1)
+  const int32_t* ref_row_ptr;  // reference working set of the controls
+  const int32_t* ref_col_idx;
+  int64_t ref_cap;
   uint32_t* err;
 };
 

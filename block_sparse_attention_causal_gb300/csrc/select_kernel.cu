@@ -13,6 +13,12 @@
 //      of lane l is block 32*jj + l, so the ballot at step jj is word jj of
 //      the row's support bitmask (kept by lane jj). Steps are OR-ed, then the
 //      sink / diagonal blocks added.
+//      The same kernel builds the two early-static controls of WISE's
+//      Appendix B ("Intervention controls") from one step's masses and a
+//      reference working set: MassMatched (Eqs 20-21) replaces eta by the
+//      row's mass covered by the reference, summed in the same fixed point;
+//      SizeMatched (Eq 22) keeps the reference's block count k and finds the
+//      k-th mass with a bitwise search on counts instead of sums.
 //  finalize_kernel    : row_ptr (each CTA adds up the counts before its rows),
 //      nnz, ascending col_idx from the bitmasks, and the late-step work order:
 //      per L2 group of (batch, head) slices, units sorted by number of listed
@@ -43,6 +49,10 @@ struct SelectParams {
   int32_t units_per_bh;
   int32_t qb_per_unit;  // query blocks per work unit (128 / block)
   int32_t group_heads;
+  int32_t mode;                // 0: Eq 6 with eta; 1: MassMatched; 2: SizeMatched
+  const int32_t* ref_row_ptr;  // reference working set (modes 1 and 2)
+  const int32_t* ref_col_idx;
+  int64_t ref_cap;
   uint32_t* err;
 };
 
@@ -69,13 +79,38 @@ __device__ __forceinline__ int warp_sum32(int v) {
 // 8 warps per CTA, one row per warp; NJ rounds of 32 blocks cover nb <= 32 NJ.
 template <int NJ>
 __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  __shared__ uint32_t refbits[8][32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t row = (int64_t)blockIdx.x * 8 + wid;
   const int64_t rows = (int64_t)p.bh_count * p.nb;
   if (row >= rows) return;
   const int bh = (int)(row / p.nb);
   const int q = (int)(row % p.nb);
   const int nadm = q + 1;  // admissible key blocks 0..q
+  // Controls: the reference row as a bitmask (entries outside 0..q flagged and
+  // skipped; repeated entries count once); in_ref[jj] is this lane's block.
+  bool in_ref[NJ];
+  int ref_k = 0;
+  if (p.mode != 0) {
+    refbits[wid][lane] = 0u;
+    __syncwarp();
+    int32_t a = __ldg(p.ref_row_ptr + row), b = __ldg(p.ref_row_ptr + row + 1);
+    bool bad = false;
+    if (a < 0 || b < a || (int64_t)b > p.ref_cap) {
+      a = b = 0;
+      bad = true;
+    }
+    for (int32_t j = a + lane; j < b; j += 32) {
+      const int32_t c = __ldg(p.ref_col_idx + j);
+      if (c >= 0 && c <= q) atomicOr(&refbits[wid][c >> 5], 1u << (c & 31));
+      else bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, kErrBadSupport);
+    __syncwarp();
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) in_ref[jj] = (refbits[wid][jj] >> lane) & 1u;
+    ref_k = warp_sum32(__popc(refbits[wid][lane]));
+  }
   uint32_t word = 0;  // word `lane` of the row's union bitmask
   for (int w = 0; w < p.window; ++w) {
     const float* src = p.mass + (((int64_t)w * p.bh_count + bh) * p.nb + q) * p.nb;
@@ -95,7 +130,48 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) max_pos = max(max_pos, (int64_t)__shfl_xor_sync(0xffffffffu, max_pos, off));
     uint32_t sel_word_mine = 0;  // the word this lane will hold (word index = lane)
-    if (total_pos < p.target_fx) {
+    int64_t target = p.target_fx;
+    if (p.mode == 1) {  // MassMatched: the mass the reference covers at this step
+      int64_t t = 0;
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) t += (in_ref[jj] && fx[jj] > 0) ? fx[jj] : 0;
+      target = warp_sum_u63(t);
+    }
+    if ((p.mode == 1 && target <= 0) || (p.mode == 2 && ref_k == 0)) {
+      // an empty reference (or one without mass) selects nothing
+    } else if (p.mode == 2) {
+      // SizeMatched: the ref_k largest masses; v = the largest value with at
+      // least ref_k admissible blocks >= v
+      int64_t v = 0;
+      if (ref_k < nadm) {
+        for (int bit = 63 - __clzll(max_pos > 0 ? max_pos : 1); bit >= 0; --bit) {
+          const int64_t cand = v | (int64_t(1) << bit);
+          int cnt = 0;
+#pragma unroll
+          for (int jj = 0; jj < NJ; ++jj) cnt += (fx[jj] >= cand) ? 1 : 0;
+          if (warp_sum32(cnt) >= ref_k) v = cand;
+        }
+      }
+      int c_above = 0;
+      const int64_t hi = v + p.tol_fx, lo = v - p.tol_fx;
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) c_above += (fx[jj] != INT64_MIN && fx[jj] > hi) ? 1 : 0;
+      c_above = warp_sum32(c_above);
+      const int k = min(ref_k, nadm);
+      int slots = k - c_above;  // filled from the near-tie group, lowest index first
+      int taken = 0;
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) {
+        const bool above = fx[jj] != INT64_MIN && fx[jj] > hi;
+        const bool near = fx[jj] != INT64_MIN && fx[jj] >= lo && fx[jj] <= hi;
+        const uint32_t nb_bal = __ballot_sync(0xffffffffu, near);
+        const int rank = taken + __popc(nb_bal & ((1u << lane) - 1u));
+        const bool pick = above || (near && rank < slots);
+        taken += __popc(nb_bal);
+        const uint32_t bal = __ballot_sync(0xffffffffu, pick);
+        if (lane == jj) sel_word_mine = bal;
+      }
+    } else if (total_pos < target) {
       // Eq 6 cannot reach eta: every admissible block.
 #pragma unroll
       for (int jj = 0; jj < NJ; ++jj) {
@@ -112,7 +188,7 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
 #pragma unroll
         for (int jj = 0; jj < NJ; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
         sacc = warp_sum_u63(sacc);
-        if (sacc >= p.target_fx) v = cand;
+        if (sacc >= target) v = cand;
       }
       int64_t s_gt = 0;
       int c_gt = 0, c_above = 0;
@@ -126,7 +202,7 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
       s_gt = warp_sum64(s_gt);
       c_gt = warp_sum32(c_gt);
       c_above = warp_sum32(c_above);
-      const int64_t need = p.target_fx - s_gt;  // > 0
+      const int64_t need = target - s_gt;  // > 0
       const int m = (int)((need + v - 1) / v);
       const int k = c_gt + m;
       int slots = k - c_above;  // filled from the near-tie group, lowest index first
@@ -276,6 +352,10 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   p.units_per_bh = s.units_per_bh;
   p.qb_per_unit = s.qb_per_unit;
   p.group_heads = s.group_heads;
+  p.mode = s.mode;
+  p.ref_row_ptr = s.ref_row_ptr;
+  p.ref_col_idx = s.ref_col_idx;
+  p.ref_cap = s.ref_cap;
   p.err = s.err;
   const int64_t rows = (int64_t)s.bh_count * s.nb;
   const unsigned grid_rows = (unsigned)((rows + 7) / 8);

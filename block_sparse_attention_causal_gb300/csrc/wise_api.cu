@@ -293,6 +293,7 @@ int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int
   const int64_t rows = s.bh * s.nb;
   const int64_t words = (s.nb + 31) / 32;
   SelectLaunch sl;
+  memset(&sl, 0, sizeof(sl));
   sl.mass = block_mass;
   sl.window = window;
   sl.bh_count = (int32_t)s.bh;
@@ -334,6 +335,7 @@ int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_m
   const int64_t rows = s.bh * s.nb;
   const int64_t words = (s.nb + 31) / 32;
   SelectLaunch sl;
+  memset(&sl, 0, sizeof(sl));
   sl.mass = block_mass;
   sl.window = window;
   sl.bh_count = (int32_t)s.bh;
@@ -419,6 +421,55 @@ int wise_support_jaccard(const wise_attn_desc* desc, const int32_t* row_ptr_a, c
   d.batch_value = batch_jaccard;
   d.err = err;
   return launch_jaccard(d, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
+}
+
+int wise_select_control(const wise_attn_desc* desc, const float* block_mass, int32_t mode,
+                        const int32_t* ref_row_ptr, const int32_t* ref_col_idx, int64_t ref_capacity, uint32_t flags,
+                        int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity, int32_t* tile_order, int32_t* nnz,
+                        void* workspace, size_t workspace_bytes, wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (mode != WISE_CONTROL_MASS_MATCHED && mode != WISE_CONTROL_SIZE_MATCHED) return WISE_ERR_INVALID_ARGUMENT;
+  if (!block_mass || !ref_row_ptr || !ref_col_idx || !row_ptr || !col_idx || ref_capacity < 0 || (flags & ~3u))
+    return WISE_ERR_INVALID_ARGUMENT;
+  if (col_capacity < wise_support_capacity(desc)) return WISE_ERR_BAD_SUPPORT;
+  const size_t need = wise_select_workspace(desc, 1);
+  if (!workspace || workspace_bytes < need) return WISE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) || (reinterpret_cast<uintptr_t>(block_mass) & 3u) ||
+      (reinterpret_cast<uintptr_t>(row_ptr) & 3u) || (reinterpret_cast<uintptr_t>(col_idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(ref_row_ptr) & 3u) || (reinterpret_cast<uintptr_t>(ref_col_idx) & 3u))
+    return WISE_ERR_ALIGNMENT;
+  uint32_t* err = error_word();
+  if (!err) return WISE_ERR_CUDA;
+  const Shape s = shape_of(desc);
+  const int64_t rows = s.bh * s.nb;
+  const int64_t words = (s.nb + 31) / 32;
+  SelectLaunch sl;
+  memset(&sl, 0, sizeof(sl));
+  sl.mass = block_mass;
+  sl.window = 1;
+  sl.bh_count = (int32_t)s.bh;
+  sl.nb = s.nb;
+  sl.target_fx = 0;
+  sl.tol_fx = fixed_point(1e-6);
+  sl.flags = flags;
+  sl.bits = static_cast<uint32_t*>(workspace);
+  sl.counts = reinterpret_cast<int32_t*>(static_cast<uint32_t*>(workspace) + rows * words);
+  sl.row_ptr = row_ptr;
+  sl.col_idx = col_idx;
+  sl.col_cap = col_capacity;
+  sl.nnz = nnz;
+  sl.tile_order = tile_order;
+  sl.units_per_bh = s.n_qtiles;
+  sl.qb_per_unit = 128 / s.bn;
+  sl.group_heads = s.group_heads;
+  sl.mode = mode;
+  sl.ref_row_ptr = ref_row_ptr;
+  sl.ref_col_idx = ref_col_idx;
+  sl.ref_cap = ref_capacity;
+  sl.err = err;
+  cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
 }
 
 int wise_validate_support(const wise_attn_desc* desc, const int32_t* row_ptr, const int32_t* col_idx,

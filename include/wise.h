@@ -16,6 +16,8 @@
  *   wise_attn_sparse     §5.2 Eqs 7-8 (late-step attention restricted to the
  *                        reused support; Q/K/V and the within-support softmax
  *                        are recomputed on every call);
+ *   wise_select_control  the MassMatched and SizeMatched controls of
+ *                        Appendix B Eqs 20-22;
  *   wise_support_retained_mass, wise_support_jaccard
  *                        the support diagnostics of Appendix B ("retained
  *                        future attention mass") and Appendix C.2 Eq 24
@@ -213,6 +215,35 @@ int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_m
 int wise_attn_sparse(const wise_attn_desc* desc, const void* q, const void* k, const void* v,
                      const int32_t* row_ptr, const int32_t* col_idx, int64_t col_capacity,
                      const int32_t* tile_order, void* o, float* lse, wise_stream_t stream);
+
+/*
+ * wise_select_control -- the early-static support controls of WISE Appendix B
+ * ("Intervention controls"), built from ONE step's masses (the pages use the
+ * first recurrent step) and a reference working set (WISE's own):
+ *   WISE_CONTROL_MASS_MATCHED (Eqs 20-21): per query block q, the smallest
+ *       set of highest-mass admissible blocks of this step whose cumulative
+ *       mass reaches m_q, the mass of this step that the reference row covers
+ *       (summed in the same 2^-52 fixed point as Eq 6);
+ *   WISE_CONTROL_SIZE_MATCHED (Eq 22): the |reference row| highest-mass
+ *       admissible blocks of this step (TopK).
+ * Order, near-tie rule and output are those of wise_select_support; the
+ * Static-95 control (Eq 19) is wise_select_support itself with window 1,
+ * eta = 0.95 and the first step's masses.
+ *   block_mass   : [batch, heads, nb, nb] float32 masses of the step (device).
+ *   mode         : WISE_CONTROL_MASS_MATCHED or WISE_CONTROL_SIZE_MATCHED.
+ *   ref_row_ptr, ref_col_idx, ref_capacity : the reference support CSR
+ *                  (device); repeated entries count once, entries outside
+ *                  0 <= b <= q are skipped and flagged.
+ *   flags        : WISE_SUPPORT_SINK / _DIAG blocks added afterwards (0 for
+ *                  the pages' definitions).
+ *   row_ptr .. nnz, workspace : as in wise_select_support with window = 1
+ *                  (workspace of wise_select_workspace(desc, 1) bytes).
+ */
+enum { WISE_CONTROL_MASS_MATCHED = 1, WISE_CONTROL_SIZE_MATCHED = 2 };
+int wise_select_control(const wise_attn_desc* desc, const float* block_mass, int32_t mode,
+                        const int32_t* ref_row_ptr, const int32_t* ref_col_idx, int64_t ref_capacity, uint32_t flags,
+                        int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity, int32_t* tile_order, int32_t* nnz,
+                        void* workspace, size_t workspace_bytes, wise_stream_t stream);
 
 /*
  * wise_support_retained_mass -- retained future attention mass (WISE

@@ -415,3 +415,43 @@ def test_grouped_query_discover_and_sparse(shape):
     o_ref, lse_ref = O.sparse(x[0].astype(np.float64), x[1].astype(np.float64), x[2].astype(np.float64), blk, rp, ci)
     _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
     _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+
+
+# --------------------------------------- App. B support controls (Eqs 19-22) ----
+
+@pytest.mark.parametrize("case", [(1, 2, 4, 64), (2, 3, 32, 128), (1, 1, 300, 64), (1, 1, 1024, 64)],
+                         ids=lambda c: "B%d_H%d_nb%d_blk%d" % c)
+@pytest.mark.parametrize("mode", ["mass", "size"])
+@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("flags", [0, 3])
+def test_controls_bit_exact_on_same_masses(case, mode, ties, flags):
+    """MassMatched / SizeMatched rows from one step's masses and a reference
+    working set (the WISE selection over three other steps, with some rows
+    emptied), bit for bit against the oracle."""
+    b, h, nb, blk = case
+    m = _random_masses(4, b, h, nb, seed=nb * 3 + b, ties=ties)
+    ref = wise.select_support(torch.from_numpy(m[1:]).contiguous().cuda(), nb * blk, 64, blk, 0.9, 0)
+    rows = ref.to_lists()
+    rng = np.random.default_rng(nb)
+    rows = [[] if rng.random() < 0.1 else r for r in rows]  # empty reference rows select nothing
+    ref = wise.support_from_lists(rows, b, h, nb * blk, 64, blk)
+    got = wise.select_control(torch.from_numpy(np.ascontiguousarray(m[0])).cuda(), ref, mode, flags)
+    wise.check_device()
+    want = []
+    for bi in range(b):
+        for hi in range(h):
+            base = (bi * h + hi) * nb
+            want += O.control_set(m[0, bi, hi].astype(np.float64), rows[base:base + nb], mode, flags)
+    assert got.to_lists() == want
+    _check_tile_order(got)
+
+
+def test_static95_is_a_one_step_window():
+    """Static-95 (Eq 19): select_support over the first step alone at eta 0.95."""
+    b, h, nb, blk = 1, 2, 48, 64
+    m = _random_masses(1, b, h, nb, seed=95)
+    sup = wise.select_support(torch.from_numpy(m).cuda(), nb * blk, 64, blk, 0.95, 0)
+    want = []
+    for hi in range(h):
+        want += [sorted(O.step_support(m[0, 0, hi, q].astype(np.float64), q, 0.95)) for q in range(nb)]
+    assert sup.to_lists() == want

@@ -384,12 +384,24 @@ def support_quality(wise, cfg, dev_in, frozen, masses, ws, o, lse):
     adj = [float(wise.support_jaccard(rolling[t - 1], rolling[t])[2].mean().item()) for t in range(1, cfg.steps)]
     retained = [float(wise.retained_mass(step_mass[t], frozen)[1].mean().item()) for t in range(td, cfg.steps)]
     drift = float(wise.support_jaccard(rolling[td - 1], rolling[cfg.steps - 1])[2].mean().item())
+    # the early-static controls of App. B (Eqs 19-22) against the same future steps
+    static95 = wise.select_support(step_mass[0][None].contiguous(), n, d, blk, 0.95, 0)
+    controls = {"static95": static95, "mass_matched": wise.select_control(step_mass[0], frozen, "mass"),
+                "size_matched": wise.select_control(step_mass[0], frozen, "size")}
+    causal_blocks = B * H * cfg.n_blocks * (cfg.n_blocks + 1) / 2
+    ctl = {}
+    for name, sup in controls.items():
+        kept = [float(wise.retained_mass(step_mass[t], sup)[1].mean().item()) for t in range(td, cfg.steps)]
+        ctl[name] = {"retained_future_mass": round(sum(kept) / len(kept), 5),
+                     "density": round(int(sup.nnz.item()) / causal_blocks, 4)}
     wise.check_device()
     return {"retained_future_mass": {"mean": round(sum(retained) / len(retained), 5),
                                      "per_late_step": [round(x, 5) for x in retained]},
             "rolling_jaccard_adjacent": [round(x, 5) for x in adj],
             "rolling_jaccard_at_td": round(adj[td - 2], 5) if td >= 2 else None,
             "drift_jaccard_td_to_T": round(drift, 5),
+            "wise_density": round(int(frozen.nnz.item()) / causal_blocks, 4),
+            "controls": ctl,
             "definitions": "retained mass: App. B; rolling sets: Eq 23 (0-indexed steps); Jaccard: Eq 24"}
 
 

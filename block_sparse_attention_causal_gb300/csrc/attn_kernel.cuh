@@ -945,37 +945,34 @@ __global__ void __launch_bounds__(512, 1)
       if (p.lse != nullptr && row_valid) p.lse[grow] = lse2 * 0.69314718055994531f;
       if (want_mass) {
         // Eq 5: r_qb = (1/B) * sum over the block's rows of 2^(lam_ib - lse2_i).
-        // Partial sums per warp go through the stream's statistics area (read
-        // above), 64 entries at a time; blocks past the unit's entries are zero.
-        float* part = st;
-        const float* lam = p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + r;
-        const bool row_has = row_valid && lse2 > -INFINITY;
-        for (int c0 = 0; c0 < cnt; c0 += 64) {
-          const int c1 = min(cnt, c0 + 64);
-          for (int e = c0; e < c1; ++e) {
-            float a = row_has ? fast_exp2(lam[(size_t)e * 128] - lse2) : 0.f;
+        // Warp `quarter` takes entries quarter, quarter + 4, ...; lane l reads
+        // rows 4l..4l+3 of an entry as one float4, so the loads of different
+        // entries do not wait on each other, and a (half-)warp reduction gives
+        // the block's sum. lse2 of the rows comes from the statistics area.
+        const float* lamt = p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE);
+        float l2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = 4 * lane + i;
+          const float v = st[row];
+          // rows past n, or with no admissible key, contribute nothing
+          l2[i] = (t * 128 + row < p.n && v > -INFINITY) ? v : INFINITY;
+        }
+#pragma unroll 4
+        for (int e = quarter; e < cnt; e += 4) {
+          const float4 lv = *reinterpret_cast<const float4*>(lamt + (size_t)e * 128 + 4 * lane);
+          float a = (fast_exp2(lv.x - l2[0]) + fast_exp2(lv.y - l2[1])) + (fast_exp2(lv.z - l2[2]) + fast_exp2(lv.w - l2[3]));
+          if (BN == 128) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            if (lane == 0) part[quarter * 64 + (e - c0)] = a;
+            if (lane == 0) p.mass[((size_t)bh * p.nb + t) * p.nb + e] = a * (1.f / BN);
+          } else {
+            // lanes 0-15 hold rows 0-63 (query block 2t), lanes 16-31 rows 64-127
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+            const int qb = 2 * t + (lane >> 4);
+            if ((lane & 15) == 0 && qb < p.nb) p.mass[((size_t)bh * p.nb + qb) * p.nb + e] = a * (1.f / BN);
           }
-          named_bar_sync(2, 128);
-          const int e = c0 + (r & 63);
-          if (e < c1) {
-            if (BN == 128) {
-              if (r < 64) {
-                const float v = (part[e - c0] + part[64 + e - c0]) + (part[128 + e - c0] + part[192 + e - c0]);
-                p.mass[((size_t)bh * p.nb + t) * p.nb + e] = v * (1.f / BN);
-              }
-            } else {
-              const int qq = r >> 6;
-              const int qb = 2 * t + qq;
-              if (qb < p.nb) {
-                const float v = part[(2 * qq) * 64 + e - c0] + part[(2 * qq + 1) * 64 + e - c0];
-                p.mass[((size_t)bh * p.nb + qb) * p.nb + e] = v * (1.f / BN);
-              }
-            }
-          }
-          named_bar_sync(2, 128);  // part is reused by the next chunk
         }
         for (int qq = 0; qq < C::ENT_PER_TILE; ++qq) {
           const int qb = t * C::ENT_PER_TILE + qq;

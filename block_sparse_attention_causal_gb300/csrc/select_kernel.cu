@@ -70,6 +70,11 @@ __device__ __forceinline__ int64_t warp_sum_u63(int64_t v) {
   const uint32_t c = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(u >> 42));
   return static_cast<int64_t>(a) + (static_cast<int64_t>(b) << 21) + (static_cast<int64_t>(c) << 42);
 }
+__device__ __forceinline__ int64_t warp_max64(int64_t v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = max(v, (int64_t)__shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
 __device__ __forceinline__ int warp_sum32(int v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -144,12 +149,20 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
       // least ref_k admissible blocks >= v
       int64_t v = 0;
       if (ref_k < nadm) {
-        for (int bit = 63 - __clzll(max_pos > 0 ? max_pos : 1); bit >= 0; --bit) {
-          const int64_t cand = v | (int64_t(1) << bit);
-          int cnt = 0;
+        if (NJ == 1) {
+          // one value per lane: v = the largest value with >= ref_k values >= it
+          int c = 0;
+#pragma unroll 8
+          for (int j = 0; j < 32; ++j) c += (__shfl_sync(0xffffffffu, fx[0], j) >= fx[0]) ? 1 : 0;
+          v = warp_max64((fx[0] != INT64_MIN && c >= ref_k) ? fx[0] : 0);
+        } else {
+          for (int bit = 63 - __clzll(max_pos > 0 ? max_pos : 1); bit >= 0; --bit) {
+            const int64_t cand = v | (int64_t(1) << bit);
+            int cnt = 0;
 #pragma unroll
-          for (int jj = 0; jj < NJ; ++jj) cnt += (fx[jj] >= cand) ? 1 : 0;
-          if (warp_sum32(cnt) >= ref_k) v = cand;
+            for (int jj = 0; jj < NJ; ++jj) cnt += (fx[jj] >= cand) ? 1 : 0;
+            if (warp_sum32(cnt) >= ref_k) v = cand;
+          }
         }
       }
       int c_above = 0;
@@ -182,13 +195,26 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
       // largest v with sum_{fx >= v} fx >= target (v > 0 since target > 0);
       // v <= the largest mass, so bits above its top bit stay zero
       int64_t v = 0;
-      for (int bit = 63 - __clzll(max_pos); bit >= 0; --bit) {
-        const int64_t cand = v | (int64_t(1) << bit);
-        int64_t sacc = 0;
+      if (NJ == 1) {
+        // one value per lane: v = the largest value x with sum{>= x} >= target
+        // (the value the bitwise search below converges to)
+        const int64_t mine = fx[0];
+        int64_t acc = 0;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+          const int64_t o = __shfl_sync(0xffffffffu, mine, j);
+          acc += (o >= mine && o > 0) ? o : 0;
+        }
+        v = warp_max64((mine > 0 && acc >= target) ? mine : 0);
+      } else {
+        for (int bit = 63 - __clzll(max_pos); bit >= 0; --bit) {
+          const int64_t cand = v | (int64_t(1) << bit);
+          int64_t sacc = 0;
 #pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
-        sacc = warp_sum_u63(sacc);
-        if (sacc >= target) v = cand;
+          for (int jj = 0; jj < NJ; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
+          sacc = warp_sum_u63(sacc);
+          if (sacc >= target) v = cand;
+        }
       }
       int64_t s_gt = 0;
       int c_gt = 0, c_above = 0;
@@ -233,11 +259,17 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
 constexpr int kChunkRows = 256;  // rows per finalize CTA (one per thread)
 
 // Rank the units of one L2 group by cost (listed blocks), heaviest first, ties
-// by unit index, and write their global order.
-__device__ void order_group(const SelectParams& p, int g, int32_t* cost) {
+// by unit index, and write their global order: a stable counting sort.
+// Shared memory: cost[units] | start[maxc + 1], maxc = nb * qb_per_unit.
+__device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
   const int h0 = g * p.group_heads;
   const int gsize = min(p.group_heads, p.bh_count - h0);
   const int units = gsize * p.units_per_bh;
+  const int maxc = p.nb * p.qb_per_unit;
+  int32_t* cost = sh;
+  int32_t* start = sh + units;
+  for (int c = threadIdx.x; c <= maxc; c += blockDim.x) start[c] = 0;
+  __syncthreads();
   for (int u = threadIdx.x; u < units; u += blockDim.x) {
     const int bh = h0 + u / p.units_per_bh, pr = u % p.units_per_bh;
     int c = 0;
@@ -245,18 +277,43 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* cost) {
       const int qb = pr * p.qb_per_unit + j;
       if (qb < p.nb) c += p.counts[(int64_t)bh * p.nb + qb];
     }
+    c = min(max(c, 0), maxc);
     cost[u] = c;
+    atomicAdd(&start[c], 1);
   }
   __syncthreads();
-  const int64_t gbase = (int64_t)h0 * p.units_per_bh;
-  for (int u = threadIdx.x; u < units; u += blockDim.x) {
-    const int c = cost[u];
-    int pos = 0;
-    for (int v = 0; v < units; ++v) {
-      const int cv = cost[v];
-      pos += (cv > c || (cv == c && v < u)) ? 1 : 0;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    // start[c] = number of units with a larger cost (exclusive scan from the top)
+    int run = 0;
+    for (int top = maxc; top >= 0; top -= 32) {
+      const int c = top - lane;
+      const int h = (c >= 0) ? start[c] : 0;
+      int inc = h;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+      }
+      if (c >= 0) start[c] = run + inc - h;
+      run += __shfl_sync(0xffffffffu, inc, 31);
     }
-    p.tile_order[gbase + pos] = h0 * p.units_per_bh + u;
+    __syncwarp();
+    // place the units in index order, 32 at a time; equal costs keep index order
+    const int64_t gbase = (int64_t)h0 * p.units_per_bh;
+    for (int b = 0; b < units; b += 32) {
+      const int u = b + lane;
+      const int c = (u < units) ? cost[u] : -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, c);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int base = (u < units) ? start[c] : 0;
+      __syncwarp();
+      if (u < units) {
+        p.tile_order[gbase + base + rank] = h0 * p.units_per_bh + u;
+        if (rank == 0) start[c] = base + __popc(peers);
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -368,7 +425,8 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   else select_rows_kernel<32><<<grid_rows, 256, 0, stream>>>(p);
   const int n_chunks = (int)((rows + kChunkRows - 1) / kChunkRows);
   const int groups = s.tile_order ? (s.bh_count + s.group_heads - 1) / s.group_heads : 0;
-  const size_t shm = s.tile_order ? (size_t)s.group_heads * s.units_per_bh * sizeof(int32_t) : 0;
+  const size_t shm =
+      s.tile_order ? ((size_t)s.group_heads * s.units_per_bh + (size_t)s.nb * s.qb_per_unit + 1) * sizeof(int32_t) : 0;
   if (shm > 40 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
     if (e != cudaSuccess) return e;

@@ -133,7 +133,7 @@ class ClockSampler:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("attn_kernel.cuh", "ptx.cuh", "select_kernel.cu"):
+    for name in ("attn_kernel.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "block_sparse_attention_causal_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -364,11 +364,22 @@ __global__ void __launch_bounds__(kChunkRows) finalize_kernel(const SelectParams
     if (start + c > p.col_cap) atomicOr(p.err, kErrBadSupport);
   }
   __syncthreads();
-  // emit: one warp per row, lane j holds bitmask word j
-  for (int i = warp; i < kChunkRows; i += kChunkRows / 32) {
+  // emit: one warp per row, lane j holds bitmask word j; a warp's rows are
+  // i = warp + 8k, and all their words are loaded before the first is used
+  // (one round of memory latency instead of one per row)
+  constexpr int kRowsPerWarp = kChunkRows / (kChunkRows / 32);
+  uint32_t words[kRowsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k) {
+    const int64_t row = r0 + warp + k * (kChunkRows / 32);
+    words[k] = (row < rows && lane < p.nwords) ? __ldg(p.bits + row * p.nwords + lane) : 0u;
+  }
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k) {
+    const int i = warp + k * (kChunkRows / 32);
     const int64_t row = r0 + i;
     if (row >= rows) break;
-    const uint32_t word = (lane < p.nwords) ? p.bits[row * p.nwords + lane] : 0u;
+    const uint32_t word = words[k];
     const int wc = __popc(word);
     int excl = wc;
 #pragma unroll
@@ -376,9 +387,10 @@ __global__ void __launch_bounds__(kChunkRows) finalize_kernel(const SelectParams
       const int y = __shfl_up_sync(0xffffffffu, excl, off);
       if (lane >= off) excl += y;
     }
+    const int total = __shfl_sync(0xffffffffu, excl, 31);
     excl -= wc;
     const int64_t st = start_s[i];
-    if (st + p.counts[row] > p.col_cap) continue;  // flagged above
+    if (st + total > p.col_cap) continue;  // flagged above
     uint32_t w = word;
     int64_t pos = st + excl;
     while (w) {

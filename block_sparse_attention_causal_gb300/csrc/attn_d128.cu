@@ -37,6 +37,7 @@ cudaError_t launch_one(const CUtensorMap* m, const AttnParams& p, cudaStream_t s
 
 cudaError_t launch_attn_d128(int block, bool sparse, const CUtensorMap* maps, const AttnParams& p, cudaStream_t st) {
   if (block == 128) return sparse ? launch_one<128, 128, true>(maps, p, st) : launch_one<128, 128, false>(maps, p, st);
+  if (block == 32) return sparse ? launch_one<128, 32, true>(maps, p, st) : launch_one<128, 32, false>(maps, p, st);
   return sparse ? launch_one<128, 64, true>(maps, p, st) : launch_one<128, 64, false>(maps, p, st);
 }
 

@@ -18,13 +18,19 @@
 //   warp 0      scheduler: claims units, walks their key-block lists and
 //               publishes one record per entry (plus an end marker per stream)
 //   warp 1      TMA loads of Q (per unit, one buffer per stream), K and V
-//   warp 2      issues every MMA from one thread: for each record in order,
-//               O_s += P_s V, then S_s = Q_s K^T of that stream's next entry
-//   warp 3      TMEM allocation
+//   warps 2, 3  MMA issue for stream 0 / stream 1 (warp 3 also allocates
+//               TMEM): for each record of the stream, O_s += P_s V, then
+//               S_s = Q_s K^T of the stream's next entry
 //   warps 4-7   softmax of stream 0, one score row per thread
 //   warps 8-11  softmax of stream 1
 //   warps 12-15 epilogue of both streams: O normalisation and store, LSE,
 //               block masses
+// Entries are 128 keys wide for blocks of 128 and of 32, 64 keys for blocks
+// of 64. With blocks of 32, a discovery entry is a contiguous 128-key span
+// (four key blocks, with one Eq 5 partial sum per block and row), and a
+// sparse entry gathers any four key blocks listed by the tile's four query
+// blocks (32-row TMA boxes), with a per-(query block, slot) mask; each
+// softmax warp owns one 32-row query block, so the mask is warp-uniform.
 // TMEM: S_0 | S_1 | O_0 | O_1. P (bf16) is written over S_s by the softmax
 // and read from TMEM by the PV MMA; the next S_s of the same stream is issued
 // by the same thread right after that PV MMA, and tcgen05 MMAs issued by one
@@ -60,24 +66,61 @@ enum : uint32_t {
   kEntRows1 = 32u,  // ... query block 1 (BN = 64 only)
 };
 
+// Entry records: word 0 is the tag (record index + 1), written last; tag and
+// info are read together with one 64-bit acquire load.
+struct __align__(16) EntryRec {
+  uint32_t tag;
+  uint32_t info;   // flags | query-block bits << 4 | block index << 8
+  uint32_t krow;   // global row of the key block's first key in K/V (TMA coordinate)
+  uint32_t unit;   // unit id = bh * n_qtiles + tile
+};
+// Record of a gathered entry (sparse steps with blocks of 32): up to four
+// listed key blocks in ascending order; unused slots repeat the last block
+// and are masked for every row.
+struct __align__(16) GatherRec {
+  uint32_t tag;
+  uint32_t info;    // flags | slot mask << 8: bit 4j + c = query block j of the tile lists slot c's block
+  uint32_t krow;    // key blocks of slots 0 and 1 (16 bits each)
+  uint32_t unit;    // unit id = bh * n_qtiles + tile
+  uint32_t kb23;    // key blocks of slots 2 and 3
+  uint32_t kvrow0;  // first K/V row of the unit's key/value head
+  uint32_t pad[2];
+};
+__device__ __forceinline__ int gather_kb(const GatherRec& e, int c) {
+  const uint32_t w = (c < 2) ? e.krow : e.kb23;
+  return (int)((c & 1) ? (w >> 16) : (w & 0xffffu));
+}
+
+template <bool B, class T, class F>
+struct pick_type {
+  using type = T;
+};
+template <class T, class F>
+struct pick_type<false, T, F> {
+  using type = F;
+};
+
 template <int D, int BN, bool SPARSE>
 struct AttnCfg {
   static_assert(D == 64 || D == 96 || D == 128, "head_dim");
-  static_assert(BN == 64 || BN == 128, "block");
+  static_assert(BN == 32 || BN == 64 || BN == 128, "block");
+  static constexpr int KW = (BN == 32) ? 128 : BN;       // keys per entry (one K/V tile)
+  static constexpr bool GATHER = SPARSE && BN == 32;      // entries gather four listed 32-key blocks
+  using Rec = typename pick_type<GATHER, GatherRec, EntryRec>::type;
   static constexpr int CH = (D == 96) ? 32 : 64;         // elements per swizzled smem row
   static constexpr int NCH = D / CH;                     // TMA boxes per tile
   static constexpr uint32_t SWZ = (CH == 64) ? 2u : 4u;  // descriptor code: 128B / 64B swizzle
   static constexpr uint32_t ROWB = CH * 2;               // bytes per swizzled row
   static constexpr uint32_t Q_BYTES = 128u * D * 2u;
-  static constexpr uint32_t KV_BYTES = (uint32_t)BN * D * 2u;
+  static constexpr uint32_t KV_BYTES = (uint32_t)KW * D * 2u;
   static constexpr int THREADS = 512;
-  static constexpr int META = 32;     // entry records in flight
+  static constexpr int META = GATHER ? 16 : 32;  // entry records in flight
   static constexpr int MAX_NB = 1024;
   static constexpr int ENT_PER_TILE = 128 / BN;  // query blocks per 128-row tile
   // per stream: lse2[128], inv_l[128], unit, entries (+ padding)
   static constexpr int ST_STRIDE = 2 * 128 + 8;
   static constexpr uint32_t STATS_BYTES = 2u * ST_STRIDE * 4u;
-  static constexpr uint32_t META_BYTES = META * 16u;
+  static constexpr uint32_t META_BYTES = META * (uint32_t)sizeof(Rec);
   static constexpr int NBAR_FIXED = 8 * 2 + 2 + 8;
   static constexpr uint32_t MISC_BYTES = 64;
   static constexpr uint32_t SMEM_LIMIT = 232448u;  // 227 KB per CTA
@@ -97,6 +140,7 @@ struct AttnCfg {
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
   static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle atoms");
+  static_assert(OFF_META % 16 == 0, "records");
   static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t s_col(int s) { return 128u * (uint32_t)s; }
   __host__ __device__ static constexpr uint32_t o_col(int s) { return 256u + (uint32_t)(s * D); }
@@ -199,20 +243,11 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return mbar_wait<TAG>(bar, parity, &dummy_abort, err);
 }
 
-// Entry records: word 0 is the tag (record index + 1), written last; tag and
-// info are read together with one 64-bit acquire load.
-struct __align__(16) EntryRec {
-  uint32_t tag;
-  uint32_t info;   // flags | block index << 8
-  uint32_t krow;   // global row of the key block's first key in K/V (TMA coordinate)
-  uint32_t unit;   // unit id = bh * n_qtiles + tile
-};
-
 // Wait until record j is published; false on abort/timeout or if the ring
 // was overrun (which the scheduler's flow control rules out). The spin is out
 // of line; the common case (already published) is one load and a compare.
-template <int TAG>
-static __device__ __noinline__ bool wait_entry_slow(EntryRec* r, uint32_t j, volatile int* abort_flag, uint32_t* err) {
+template <int TAG, class R>
+static __device__ __noinline__ bool wait_entry_slow(R* r, uint32_t j, volatile int* abort_flag, uint32_t* err) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     const uint32_t tag = ld_acquire_smem(&r->tag);
@@ -232,11 +267,21 @@ static __device__ __noinline__ bool wait_entry_slow(EntryRec* r, uint32_t j, vol
     }
   }
 }
-// FULL: also read krow and unit (tag and info always).
-template <int TAG, bool FULL>
-__device__ __forceinline__ bool wait_entry(EntryRec* ring, int meta, uint32_t j, EntryRec& out,
-                                           volatile int* abort_flag, uint32_t* err) {
-  EntryRec* r = ring + (j % (uint32_t)meta);
+__device__ __forceinline__ void read_rest(const EntryRec* r, EntryRec& out) {
+  out.krow = r->krow;
+  out.unit = r->unit;
+}
+__device__ __forceinline__ void read_rest(const GatherRec* r, GatherRec& out) {
+  out.krow = r->krow;
+  out.unit = r->unit;
+  out.kb23 = r->kb23;
+  out.kvrow0 = r->kvrow0;
+}
+// FULL: also read the rest of the record (tag and info always).
+template <int TAG, bool FULL, class R>
+__device__ __forceinline__ bool wait_entry(R* ring, int meta, uint32_t j, R& out, volatile int* abort_flag,
+                                           uint32_t* err) {
+  R* r = ring + (j % (uint32_t)meta);
   uint64_t ti = ld_acquire_smem_b64(&r->tag);
   if ((uint32_t)ti != j + 1u) {
     if (!wait_entry_slow<TAG>(r, j, abort_flag, err)) return false;
@@ -244,10 +289,7 @@ __device__ __forceinline__ bool wait_entry(EntryRec* ring, int meta, uint32_t j,
   }
   out.tag = j + 1u;
   out.info = (uint32_t)(ti >> 32);
-  if (FULL) {
-    out.krow = r->krow;
-    out.unit = r->unit;
-  }
+  if (FULL) read_rest(r, out);
   return true;
 }
 
@@ -300,6 +342,214 @@ __device__ __forceinline__ void sched_slot_done(const AttnParams& p) {
   }
 }
 
+// ------------------------------------------------ gathered entries (B = 32)
+
+// Lane l's word of the key blocks listed by one CSR row (query block qb):
+// bit i is key block 32 l + i. [a, b) is the row's range in col_idx, v the
+// list's first 32 values (one per lane, INT32_MAX past b). Values outside
+// [0, qb] are skipped; they and values that do not ascend set `bad`.
+__device__ __forceinline__ uint32_t gather_list_bits(const AttnParams& p, int32_t a, int32_t b, int qb, int32_t v,
+                                                     int lane, bool& bad) {
+  uint32_t word = 0u;
+  int32_t prev = -1;
+  for (int32_t base = a; base < b; base += 32) {
+    if (base != a) v = (base + lane < b) ? __ldg(p.col_idx + base + lane) : INT32_MAX;
+    const bool in = base + lane < b;
+    int32_t pv = __shfl_up_sync(0xffffffffu, v, 1);
+    if (lane == 0) pv = prev;
+    const bool ok = in && v >= 0 && v > pv && v <= qb;
+    if (in && !ok) bad = true;
+    // OR each value's bit into the word of the lane that owns it, one
+    // target word per round
+    uint32_t pend = __ballot_sync(0xffffffffu, ok);
+    while (pend != 0u) {
+      const int tgt = __shfl_sync(0xffffffffu, v >> 5, __ffs(pend) - 1);
+      const bool mine = ok && (v >> 5) == tgt;
+      const uint32_t grp = __ballot_sync(0xffffffffu, mine);
+      const uint32_t bits = __reduce_or_sync(0xffffffffu, mine ? (1u << (v & 31)) : 0u);
+      if (lane == tgt) word |= bits;
+      pend &= ~grp;
+    }
+    prev = __shfl_sync(0xffffffffu, v, 31);
+  }
+  return word;
+}
+
+// The scheduler of sparse steps with blocks of 32, run by the whole warp.
+// A claimed unit's four CSR rows become per-lane bit words; each entry takes
+// the next four blocks of their union in ascending order, with the 4 x 4
+// mask of which query block lists which slot. Flow control and the order of
+// the two streams' records are those of the scheduler of the other variants.
+template <class C>
+__device__ __forceinline__ void gather_scheduler(const AttnParams& p, const CUtensorMap* tm_q, GatherRec* meta,
+                                                 uint32_t* qpos0, uint32_t* qpos1, volatile int* abort_flag,
+                                                 int lane, int d) {
+  constexpr uint32_t FULLM = 0xffffffffu;
+  constexpr uint32_t AHEAD = 10u;
+  static_assert(AHEAD + 4u <= (uint32_t)C::META, "record ring");
+  SchedSlot* sched = &g_sched[p.sched_slot];
+  uint32_t j = 0;  // records published
+  // publish record j once j < min(qpos0, qpos1) + AHEAD (lane 0 waits and writes)
+  auto publish = [&](uint32_t info, uint32_t krow, uint32_t unit, uint32_t kb23, uint32_t kvrow0) -> bool {
+    int good = 1;
+    if (lane == 0) {
+      if (j >= AHEAD) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t it = 0; j >= min(ld_acquire_smem(qpos0), ld_acquire_smem(qpos1)) + AHEAD; ++it) {
+          if ((it & 63u) == 63u) {
+            if (*abort_flag) {
+              good = 0;
+              break;
+            }
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicOr(p.err, kErrTimeout);
+              good = 0;
+              break;
+            }
+          }
+          __nanosleep(64);
+        }
+      }
+      if (good) {
+        GatherRec* r = meta + (j % (uint32_t)C::META);
+        r->info = info;
+        r->krow = krow;
+        r->unit = unit;
+        r->kb23 = kb23;
+        r->kvrow0 = kvrow0;
+        st_release_smem(&r->tag, j + 1u);
+      }
+    }
+    ++j;
+    return __shfl_sync(FULLM, good, 0) != 0;
+  };
+  struct GCur {
+    uint32_t w0, w1, w2, w3;  // this lane's word of the blocks listed by query blocks 0-3 of the tile
+    uint32_t rem;             // ... of their union, not yet published
+    int unit, cnt;
+    uint32_t kvrow0;  // first K/V row of the unit's key/value head
+    bool alive;
+  };
+  GCur sc0, sc1;
+  auto claim = [&](GCur& sc) -> bool {
+    for (;;) {
+      int stop = 0;
+      unsigned int x = 0u;
+      if (lane == 0) {
+        stop = *abort_flag;
+        if (!stop) x = atomicAdd(&sched->next, 1u);
+      }
+      if (__shfl_sync(FULLM, stop, 0)) return false;
+      x = __shfl_sync(FULLM, x, 0);
+      if ((int64_t)x >= p.n_units) return false;
+      const int64_t v = (p.tile_order != nullptr) ? (int64_t)__ldg(p.tile_order + x) : default_unit(x, p);
+      if (v < 0 || v >= p.n_units) {
+        if (lane == 0) atomicOr(p.err, kErrBadSupport);
+        continue;
+      }
+      const int id = (int)v;
+      const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
+      if (lane == 0)
+        for (int c = 0; c < C::NCH; ++c) tma_prefetch_l2_2d(tm_q, c * C::CH, bh * p.n + t * 128);
+      // CSR rows of query blocks 4t .. 4t + nq - 1 (row_ptr entries 0 .. nq)
+      const int qb0 = 4 * t;
+      const int nq = min(4, p.nb - qb0);
+      const int64_t row0 = (int64_t)bh * p.nb + qb0;
+      const int32_t rpv = (lane <= nq) ? __ldg(p.row_ptr + row0 + lane) : 0;
+      int32_t a[4], b[4], v0[4];
+      bool bad = false;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        a[q] = __shfl_sync(FULLM, rpv, q);
+        b[q] = __shfl_sync(FULLM, rpv, q + 1);
+        if (q >= nq) {
+          a[q] = b[q] = 0;
+        } else if (a[q] < 0 || a[q] > b[q] || (int64_t)b[q] > p.col_cap) {
+          bad = true;
+          a[q] = b[q] = 0;
+        }
+        v0[q] = (a[q] + lane < b[q]) ? __ldg(p.col_idx + a[q] + lane) : INT32_MAX;
+      }
+      sc.w0 = gather_list_bits(p, a[0], b[0], qb0 + 0, v0[0], lane, bad);
+      sc.w1 = gather_list_bits(p, a[1], b[1], qb0 + 1, v0[1], lane, bad);
+      sc.w2 = gather_list_bits(p, a[2], b[2], qb0 + 2, v0[2], lane, bad);
+      sc.w3 = gather_list_bits(p, a[3], b[3], qb0 + 3, v0[3], lane, bad);
+      sc.rem = sc.w0 | sc.w1 | sc.w2 | sc.w3;
+      if (__any_sync(FULLM, bad) && lane == 0) atomicOr(p.err, kErrBadSupport);
+      if (!__any_sync(FULLM, sc.rem != 0u)) {
+        if (lane == 0) write_empty_unit(id, p, d);
+        __syncwarp();
+        continue;
+      }
+      sc.unit = id;
+      sc.cnt = 0;
+      sc.kvrow0 = (uint32_t)(((bh / p.heads) * (p.heads / p.kv_group) + (bh % p.heads) / p.kv_group) * p.n);
+      return true;
+    }
+  };
+  // publish stream s's next entry; claim its next unit after the last one
+  auto step = [&](GCur& sc, uint32_t sflag) -> bool {
+    uint32_t mask = 0u;
+    int kb[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t who = __ballot_sync(FULLM, sc.rem != 0u);
+      if (who == 0u) {
+        kb[c] = kb[c > 0 ? c - 1 : 0];  // nothing left: repeat the last block, masked
+      } else {
+        const int src = __ffs(who) - 1;
+        const int bit = (sc.rem != 0u) ? __ffs(sc.rem) - 1 : 0;
+        const uint32_t qm = ((sc.w0 >> bit) & 1u) | (((sc.w1 >> bit) & 1u) << 1) | (((sc.w2 >> bit) & 1u) << 2) |
+                            (((sc.w3 >> bit) & 1u) << 3);
+        if (lane == src) sc.rem &= sc.rem - 1u;
+        const int bsrc = __shfl_sync(FULLM, bit, src);
+        const uint32_t qsrc = __shfl_sync(FULLM, qm, src);
+        kb[c] = 32 * src + bsrc;
+        mask |= ((qsrc & 1u) << c) | (((qsrc >> 1) & 1u) << (4 + c)) | (((qsrc >> 2) & 1u) << (8 + c)) |
+                (((qsrc >> 3) & 1u) << (12 + c));
+      }
+    }
+    const bool more = __any_sync(FULLM, sc.rem != 0u);
+    const uint32_t info = (sc.cnt == 0 ? kEntFirst : 0u) | (more ? 0u : kEntLast) | sflag | (mask << 8);
+    if (!publish(info, (uint32_t)kb[0] | ((uint32_t)kb[1] << 16), (uint32_t)sc.unit,
+                 (uint32_t)kb[2] | ((uint32_t)kb[3] << 16), sc.kvrow0))
+      return false;
+    ++sc.cnt;
+    if (more) return true;
+    sc.alive = claim(sc);
+    return sc.alive || publish(kEntMark | sflag, 0u, 0u, 0u, 0u);
+  };
+  bool ok = true;
+  sc0.alive = claim(sc0);
+  if (!sc0.alive) ok = publish(kEntMark, 0u, 0u, 0u, 0u);
+  sc1.alive = ok && claim(sc1);
+  if (ok && !sc1.alive) ok = publish(kEntMark | kEntStream, 0u, 0u, 0u, 0u);
+  int s = 0;
+  while (ok && (sc0.alive || sc1.alive)) {
+    if (s == 0 && !sc0.alive) s = 1;
+    else if (s == 1 && !sc1.alive) s = 0;
+    ok = s ? step(sc1, kEntStream) : step(sc0, 0u);
+    s ^= 1;
+  }
+}
+
+// TMA loads of one K or V tile (KV_BYTES, announced on `bar` by the caller):
+// one box per 64 (or 32) columns of the head dimension; for gathered entries,
+// four 32-row boxes per column chunk, one per slot, at the slot's key block.
+template <class C>
+__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar, const EntryRec& e) {
+  for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * C::KW * C::ROWB, tm, bar, c * C::CH, (int)e.krow);
+}
+template <class C>
+__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar, const GatherRec& e) {
+#pragma unroll
+  for (int sl = 0; sl < 4; ++sl) {
+    const int row = (int)e.kvrow0 + 32 * gather_kb(e, sl);
+    for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + (c * C::KW + sl * 32) * C::ROWB, tm, bar, c * C::CH, row);
+  }
+}
+
 template <int D, int BN, bool SPARSE>
 __global__ void __launch_bounds__(512, 1)
     wise_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -331,7 +581,8 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* k_empty = k_full + NK;   // [NK]
   uint64_t* v_full = k_empty + NK;   // [NV]
   uint64_t* v_empty = v_full + NV;   // [NV]
-  EntryRec* meta = reinterpret_cast<EntryRec*>(smem + C::OFF_META);
+  using Rec = typename C::Rec;
+  Rec* meta = reinterpret_cast<Rec*>(smem + C::OFF_META);
   float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   uint32_t* tmem_base_slot = misc;
@@ -395,7 +646,9 @@ __global__ void __launch_bounds__(512, 1)
   setmaxnreg_dec<80>();
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0) {
+    if constexpr (C::GATHER) {
+      gather_scheduler<C>(p, &tm_q, meta, qpos0, qpos1, abort_flag, lane, D);
+    } else if (lane == 0) {
       SchedSlot* sched = &g_sched[p.sched_slot];
       uint32_t j = 0;  // records published
       bool ok = true;
@@ -459,7 +712,7 @@ __global__ void __launch_bounds__(512, 1)
           const int id = (int)v;
           const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
           if (SPARSE) sc.cur.init_sparse(t, bh, p, C::ENT_PER_TILE);
-          else sc.cur.init_dense(t, p, BN);
+          else sc.cur.init_dense(t, p, C::KW);
           if (!sc.cur.next(sc.pblk, sc.pmask)) {
             if (sc.cur.bad) atomicOr(p.err, kErrBadSupport);
             write_empty_unit(id, p, D);
@@ -481,7 +734,7 @@ __global__ void __launch_bounds__(512, 1)
         const bool more = sc.cur.next(nblk, nmask);
         const uint32_t info = (sc.cnt == 0 ? kEntFirst : 0u) | (more ? 0u : kEntLast) | sflag | (sc.pmask << 4) |
                               ((uint32_t)sc.pblk << 8);
-        if (!publish(sc.kvrow0 + (uint32_t)(sc.pblk * BN), (uint32_t)sc.unit, info)) return false;
+        if (!publish(sc.kvrow0 + (uint32_t)(sc.pblk * C::KW), (uint32_t)sc.unit, info)) return false;
         if (more) {
           sc.pblk = nblk;
           sc.pmask = nmask;
@@ -527,7 +780,7 @@ __global__ void __launch_bounds__(512, 1)
       // must never wait behind an unpublished record
       const bool k_turn = kends < 2 && rk < rv + KLEAD &&
                           (rk == rv || ld_acquire_smem(&meta[rk % (uint32_t)META].tag) == rk + 1u);
-      EntryRec e;
+      Rec e;
       ok = __all_sync(0xffffffffu, wait_entry<2, true>(meta, META, k_turn ? rk : rv, e, abort_flag, p.err));
       if (!ok) break;
       if (k_turn) {
@@ -559,7 +812,7 @@ __global__ void __launch_bounds__(512, 1)
         uint8_t* dst = smem + C::OFF_K + slot * C::KV_BYTES;
         if (leader) {
           mbar_arrive_expect_tx(&k_full[slot], C::KV_BYTES);
-          for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * BN * ROWB, &tm_k, &k_full[slot], c * C::CH, (int)e.krow);
+          load_kv_tile<C>(dst, &tm_k, &k_full[slot], e);
         }
         ++nk;
       } else {
@@ -575,7 +828,7 @@ __global__ void __launch_bounds__(512, 1)
         uint8_t* dst = smem + C::OFF_V + slot * C::KV_BYTES;
         if (leader) {
           mbar_arrive_expect_tx(&v_full[slot], C::KV_BYTES);
-          for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * BN * ROWB, &tm_v, &v_full[slot], c * C::CH, (int)e.krow);
+          load_kv_tile<C>(dst, &tm_v, &v_full[slot], e);
         }
         ++nv;
       }
@@ -603,11 +856,11 @@ __global__ void __launch_bounds__(512, 1)
     const int s = warp - 2;
     const uint32_t sflag = s ? kEntStream : 0u;
     const bool leader = elect_one();
-    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, C::KW, 0, 0);
     constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
     const uint64_t qd = smem_desc(smem_u32(smem + C::OFF_Q + s * C::Q_BYTES), 16, 8 * ROWB, C::SWZ);
     const uint64_t kd_base = smem_desc(smem_u32(smem + C::OFF_K), 16, 8 * ROWB, C::SWZ);
-    const uint64_t vd_base = smem_desc(smem_u32(smem + C::OFF_V), BN * ROWB, 8 * ROWB, C::SWZ);
+    const uint64_t vd_base = smem_desc(smem_u32(smem + C::OFF_V), C::KW * ROWB, 8 * ROWB, C::SWZ);
     const uint32_t dS = tbase + C::s_col(s);
     const uint32_t dO = tbase + C::o_col(s);
     uint32_t* qpos = s ? qpos1 : qpos0;
@@ -616,7 +869,7 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
     // the stream's next record (index i, K/V ordinal o); false at its end
     // marker or on abort (then ok is false too)
-    auto next_own = [&](EntryRec& e, uint32_t& i, uint32_t& o) -> bool {
+    auto next_own = [&](Rec& e, uint32_t& i, uint32_t& o) -> bool {
       for (;;) {
         if (!__all_sync(0xffffffffu, wait_entry<3, false>(meta, META, scan, e, abort_flag, p.err))) {
           ok = false;
@@ -636,7 +889,7 @@ __global__ void __launch_bounds__(512, 1)
       }
     };
     // operands of S_s for the record with K/V ordinal o are in shared memory
-    auto wait_s = [&](const EntryRec& e, uint32_t o) -> bool {
+    auto wait_s = [&](const Rec& e, uint32_t o) -> bool {
       if (e.info & kEntFirst) {
         if (!__all_sync(0xffffffffu, mbar_wait<3>(&q_full[s], nqs & 1, abort_flag, p.err))) return false;
         ++nqs;
@@ -644,7 +897,7 @@ __global__ void __launch_bounds__(512, 1)
       return __all_sync(0xffffffffu, mbar_wait<3>(&k_full[o % NK], (o / NK) & 1, abort_flag, p.err));
     };
     // S_s = Q_s K^T for the record with K/V ordinal o (operands waited for)
-    auto issue_s = [&](const EntryRec& e, uint32_t o) {
+    auto issue_s = [&](const Rec& e, uint32_t o) {
       const int slot = (int)(o % NK);
       // descriptor start addresses advance in 16-byte units
       const uint64_t kd = kd_base + (uint64_t)((slot * C::KV_BYTES) >> 4);
@@ -652,7 +905,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int c = kk / (C::CH / 16), w = kk % (C::CH / 16);
-          umma_ss(dS, qd + (uint64_t)((c * 128 * ROWB + w * 32) >> 4), kd + (uint64_t)((c * BN * ROWB + w * 32) >> 4),
+          umma_ss(dS, qd + (uint64_t)((c * 128 * ROWB + w * 32) >> 4), kd + (uint64_t)((c * C::KW * ROWB + w * 32) >> 4),
                   IDESC_S, kk > 0);
         }
         umma_commit(&s_full[s]);
@@ -667,7 +920,7 @@ __global__ void __launch_bounds__(512, 1)
       comp[n % 8u] = ((n + 1u) << 2) | end | (uint32_t)s;
       mbar_arrive(&comp_full[n % 8u]);
     };
-    EntryRec cur;
+    Rec cur;
     uint32_t ci = 0u, co = 0u;
     bool have = next_own(cur, ci, co);
     if (have) {
@@ -681,7 +934,7 @@ __global__ void __launch_bounds__(512, 1)
       // While the softmax works on the current record: read the next record
       // and wait for every operand except P, so that the PV MMA and the next
       // S MMA issue back to back once P is written.
-      EntryRec nxt;
+      Rec nxt;
       uint32_t ni = 0u, no = 0u;
       const bool have_next = next_own(nxt, ni, no);
       if (!ok) break;
@@ -697,7 +950,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint64_t vd = vd_base + (uint64_t)((vslot * C::KV_BYTES) >> 4);
       if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
+        for (int kk = 0; kk < C::KW / 16; ++kk)
           umma_ts(dO, dS + kk * 8, vd + (uint64_t)((kk * 16 * ROWB) >> 4), IDESC_O, (first && kk == 0) ? 0u : 1u);
         umma_commit(&v_empty[vslot]);
         if (cur.info & kEntLast) {
@@ -734,15 +987,19 @@ __global__ void __launch_bounds__(512, 1)
     const float sl2 = p.scale_log2;
     const bool want_mass = (!SPARSE) && (p.mass != nullptr);
     const int half = (BN == 64) ? (r >> 6) : 0;
-    constexpr int NC = BN / 32;  // 32-column chunks of a score row
+    constexpr int NC = C::KW / 32;  // 32-column chunks of a score row
+    // blocks of 32: the fp32 row sum is taken per 32-column chunk (one Eq 5
+    // partial sum per key block in discovery); sparse steps add in the same
+    // order, so a full support reproduces discovery bit for bit
+    constexpr bool CHUNK_SUMS = (BN == 32);
     float* st = stats + s * C::ST_STRIDE;
     float m_ref = -INFINITY, l = 0.f, lt = 0.f;
     uint32_t cnt = 0, ne = 0, nst = 0;
     int t = 0, bh = 0;
     float* lam = nullptr;
     for (uint32_t rec = 0;; ++rec) {
-      EntryRec e;
-      bool ok = __all_sync(0xffffffffu, wait_entry<4, false>(meta, META, rec, e, abort_flag, p.err));
+      Rec e;
+      bool ok = __all_sync(0xffffffffu, wait_entry<4, C::GATHER>(meta, META, rec, e, abort_flag, p.err));
       if (!ok) break;
       if ((((e.info & kEntStream) != 0u) ? 1 : 0) != s) continue;
       if (e.info & kEntMark) {
@@ -761,7 +1018,7 @@ __global__ void __launch_bounds__(512, 1)
         l = 0.f;
         lt = 0.f;
         cnt = 0;
-        lam = want_mass ? p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + r : nullptr;
+        lam = want_mass ? p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE) + (CHUNK_SUMS ? 4 * r : r) : nullptr;
       }
       tc_fence_after();
       uint32_t v[NC][32];
@@ -769,16 +1026,40 @@ __global__ void __launch_bounds__(512, 1)
       for (int cc = 0; cc < NC; ++cc) tmem_ld_x32(tS + cc * 32, v[cc]);
 #pragma unroll
       for (int cc = 0; cc < NC; ++cc) tmem_wait_ld(v[cc]);
-      const int kbase = (int)(e.info >> 8) * BN;
-      const int qpos = t * 128 + r;
-      const bool row_on = (e.info >> (4 + half)) & 1u;
-      // columns c <= limit of the tile are admissible (causal mask M, working-set mask R)
-      const int limit = row_on ? ((kbase + BN - 1 > qpos) ? qpos - kbase : BN) : -1;
-      if (limit < BN - 1) {
+      if constexpr (C::GATHER) {
+        // this warp's rows are query block qb = 4t + quarter; slot c holds
+        // key block kb_c: all columns if qb lists it and kb_c < qb, columns
+        // 0..lane if kb_c == qb (causal mask M), none if qb does not list it
+        // (working-set mask R)
+        const uint32_t mq = (e.info >> (8 + 4 * quarter)) & 0xfu;
+        const int qb = 4 * t + quarter;
+        int lim[4];
+        bool any = false;
 #pragma unroll
-        for (int cc = 0; cc < NC; ++cc)
+        for (int c = 0; c < 4; ++c) {
+          const bool on = (mq >> c) & 1u;
+          const bool diag = gather_kb(e, c) == qb;
+          lim[c] = on ? (diag ? lane : 31) : -1;
+          any |= !on || diag;
+        }
+        if (any) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) v[cc][q] = (cc * 32 + q <= limit) ? v[cc][q] : __float_as_uint(-INFINITY);
+          for (int cc = 0; cc < NC; ++cc)
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[cc][q] = (q <= lim[cc]) ? v[cc][q] : __float_as_uint(-INFINITY);
+        }
+      } else {
+        const int kbase = (int)(e.info >> 8) * C::KW;
+        const int qpos = t * 128 + r;
+        const bool row_on = (e.info >> (4 + half)) & 1u;
+        // columns c <= limit of the tile are admissible (causal mask M, working-set mask R)
+        const int limit = row_on ? ((kbase + C::KW - 1 > qpos) ? qpos - kbase : C::KW) : -1;
+        if (limit < C::KW - 1) {
+#pragma unroll
+          for (int cc = 0; cc < NC; ++cc)
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[cc][q] = (cc * 32 + q <= limit) ? v[cc][q] : __float_as_uint(-INFINITY);
+        }
       }
       // row max: eight independent 3-input max chains
       float mx8[8];
@@ -807,6 +1088,7 @@ __global__ void __launch_bounds__(512, 1)
       // accumulators each). Masked entries hold -inf and give exactly 0.
       const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
       uint64_t rs2[2] = {0ull, 0ull}, rt2[2] = {0ull, 0ull};
+      float rsc[NC];  // per-chunk fp32 sums (CHUNK_SUMS)
 #pragma unroll
       for (int cc = 0; cc < NC; ++cc) {
         uint32_t pk[16];
@@ -822,6 +1104,12 @@ __global__ void __launch_bounds__(512, 1)
           add_bf16x2_to(rt2[q & 1], pk[q]);
         }
         tmem_st_x16(tS + cc * 16, pk);
+        if constexpr (CHUNK_SUMS) {
+          float a0, a1;
+          f2_unpack(fadd2(rs2[0], rs2[1]), a0, a1);
+          rsc[cc] = a0 + a1;
+          rs2[0] = rs2[1] = 0ull;
+        }
       }
       float rs, rt;
       {
@@ -831,13 +1119,26 @@ __global__ void __launch_bounds__(512, 1)
         rs = a0 + a1;
         rt = b0 + b1;
       }
+      if constexpr (CHUNK_SUMS) rs = (rsc[0] + rsc[1]) + (rsc[2] + rsc[3]);
       l = l * factor + rs;
       lt = lt * factor + rt;
       // O_s holds every PV MMA up to the previous entry (the S_s commit
       // covers them); rows whose max jumped are rescaled in place
       if (__any_sync(0xffffffffu, resc)) rescale_o(tO, D, factor);
       tmem_wait_st();
-      if (want_mass) lam[(size_t)cnt * 128] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
+      if (want_mass) {
+        if constexpr (CHUNK_SUMS) {
+          // lam_ib of the entry's four key blocks: one float4 per row
+          float4 lv;
+          lv.x = (rsc[0] > 0.f) ? m_use + fast_log2(rsc[0]) : -INFINITY;
+          lv.y = (rsc[1] > 0.f) ? m_use + fast_log2(rsc[1]) : -INFINITY;
+          lv.z = (rsc[2] > 0.f) ? m_use + fast_log2(rsc[2]) : -INFINITY;
+          lv.w = (rsc[3] > 0.f) ? m_use + fast_log2(rsc[3]) : -INFINITY;
+          reinterpret_cast<float4*>(lam)[(size_t)cnt * 128] = lv;
+        } else {
+          lam[(size_t)cnt * 128] = (rs > 0.f) ? m_use + fast_log2(rs) : -INFINITY;
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[s]);
@@ -945,40 +1246,70 @@ __global__ void __launch_bounds__(512, 1)
       if (p.lse != nullptr && row_valid) p.lse[grow] = lse2 * 0.69314718055994531f;
       if (want_mass) {
         // Eq 5: r_qb = (1/B) * sum over the block's rows of 2^(lam_ib - lse2_i).
-        // Warp `quarter` takes entries quarter, quarter + 4, ...; lane l reads
-        // rows 4l..4l+3 of an entry as one float4, so the loads of different
-        // entries do not wait on each other, and a (half-)warp reduction gives
-        // the block's sum. lse2 of the rows comes from the statistics area.
         const float* lamt = p.lam + lam_tile_offset(bh, t, p, C::ENT_PER_TILE);
-        float l2[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = 4 * lane + i;
-          const float v = st[row];
-          // rows past n, or with no admissible key, contribute nothing
-          l2[i] = (t * 128 + row < p.n && v > -INFINITY) ? v : INFINITY;
-        }
+        if constexpr (BN == 32) {
+          // warp `quarter` owns query block 4t + quarter (its 32 rows, one per
+          // lane); an entry holds four key blocks, one float4 per row. The
+          // four sums are reduced together: after the exchanges, lanes
+          // 8c .. 8c + 7 hold the sum of key block c.
+          const int qb = 4 * t + quarter;
+          const float l2 = (row_valid && lse2 > -INFINITY) ? lse2 : INFINITY;
+          const float4* lam4 = reinterpret_cast<const float4*>(lamt) + r;
+          const bool hi4 = (lane & 16) != 0, hi3 = (lane & 8) != 0;
 #pragma unroll 4
-        for (int e = quarter; e < cnt; e += 4) {
-          const float4 lv = *reinterpret_cast<const float4*>(lamt + (size_t)e * 128 + 4 * lane);
-          float a = (fast_exp2(lv.x - l2[0]) + fast_exp2(lv.y - l2[1])) + (fast_exp2(lv.z - l2[2]) + fast_exp2(lv.w - l2[3]));
-          if (BN == 128) {
+          for (int e = 0; e < cnt; ++e) {
+            const float4 lv = lam4[(size_t)e * 128];
+            const float a0 = fast_exp2(lv.x - l2), a1 = fast_exp2(lv.y - l2);
+            const float a2 = fast_exp2(lv.z - l2), a3 = fast_exp2(lv.w - l2);
+            float k0 = hi4 ? a2 : a0, k1 = hi4 ? a3 : a1;
+            k0 += __shfl_xor_sync(0xffffffffu, hi4 ? a0 : a2, 16);
+            k1 += __shfl_xor_sync(0xffffffffu, hi4 ? a1 : a3, 16);
+            float k = hi3 ? k1 : k0;
+            k += __shfl_xor_sync(0xffffffffu, hi3 ? k0 : k1, 8);
+            k += __shfl_xor_sync(0xffffffffu, k, 4);
+            k += __shfl_xor_sync(0xffffffffu, k, 2);
+            k += __shfl_xor_sync(0xffffffffu, k, 1);
+            // the last span can reach past the sequence's last key block
+            const int kb = 4 * e + (lane >> 3);
+            if ((lane & 7) == 0 && qb < p.nb && kb < p.nb) p.mass[((size_t)bh * p.nb + qb) * p.nb + kb] = k * (1.f / 32);
+          }
+        } else {
+          // Warp `quarter` takes entries quarter, quarter + 4, ...; lane l reads
+          // rows 4l..4l+3 of an entry as one float4, so the loads of different
+          // entries do not wait on each other, and a (half-)warp reduction gives
+          // the block's sum. lse2 of the rows comes from the statistics area.
+          float l2[4];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            if (lane == 0) p.mass[((size_t)bh * p.nb + t) * p.nb + e] = a * (1.f / BN);
-          } else {
-            // lanes 0-15 hold rows 0-63 (query block 2t), lanes 16-31 rows 64-127
+          for (int i = 0; i < 4; ++i) {
+            const int row = 4 * lane + i;
+            const float v = st[row];
+            // rows past n, or with no admissible key, contribute nothing
+            l2[i] = (t * 128 + row < p.n && v > -INFINITY) ? v : INFINITY;
+          }
+#pragma unroll 4
+          for (int e = quarter; e < cnt; e += 4) {
+            const float4 lv = *reinterpret_cast<const float4*>(lamt + (size_t)e * 128 + 4 * lane);
+            float a = (fast_exp2(lv.x - l2[0]) + fast_exp2(lv.y - l2[1])) + (fast_exp2(lv.z - l2[2]) + fast_exp2(lv.w - l2[3]));
+            if (BN == 128) {
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            const int qb = 2 * t + (lane >> 4);
-            if ((lane & 15) == 0 && qb < p.nb) p.mass[((size_t)bh * p.nb + qb) * p.nb + e] = a * (1.f / BN);
+              for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+              if (lane == 0) p.mass[((size_t)bh * p.nb + t) * p.nb + e] = a * (1.f / BN);
+            } else {
+              // lanes 0-15 hold rows 0-63 (query block 2t), lanes 16-31 rows 64-127
+#pragma unroll
+              for (int off = 8; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+              const int qb = 2 * t + (lane >> 4);
+              if ((lane & 15) == 0 && qb < p.nb) p.mass[((size_t)bh * p.nb + qb) * p.nb + e] = a * (1.f / BN);
+            }
           }
         }
+        // blocks past the tile's last entry (beyond the causal range)
+        const int covered = (BN == 32) ? 4 * cnt : cnt;
         for (int qq = 0; qq < C::ENT_PER_TILE; ++qq) {
           const int qb = t * C::ENT_PER_TILE + qq;
           if (qb >= p.nb) break;
           float* dst = p.mass + ((size_t)bh * p.nb + qb) * p.nb;
-          for (int e = cnt + r; e < p.nb; e += 128) dst[e] = 0.f;
+          for (int e = covered + r; e < p.nb; e += 128) dst[e] = 0.f;
         }
       }
       __syncwarp();

@@ -86,7 +86,7 @@ int check_desc(const wise_attn_desc* d) {
   if (!(d->softmax_scale >= 0.f) || isinf(d->softmax_scale)) return WISE_ERR_INVALID_ARGUMENT;
   if (d->seq_len % d->block != 0) return WISE_ERR_INVALID_ARGUMENT;
   if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128) return WISE_ERR_UNSUPPORTED;
-  if (d->block != 64 && d->block != 128) return WISE_ERR_UNSUPPORTED;
+  if (d->block != 32 && d->block != 64 && d->block != 128) return WISE_ERR_UNSUPPORTED;
   if (d->seq_len / d->block > kMaxBlocks) return WISE_ERR_UNSUPPORTED;
   const int64_t rows = (int64_t)d->batch * d->heads * d->seq_len;
   if (rows + 256 > INT32_MAX) return WISE_ERR_UNSUPPORTED;
@@ -135,9 +135,12 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
   CUtensorMap maps[3];
   const int64_t rows = s.bh * s.n;
   const int64_t kv_rows = (int64_t)desc->batch * s.kv_heads * s.n;
+  // K/V boxes: one key block (64 or 128 rows); blocks of 32 use 128-row
+  // boxes in discovery and one 32-row box per gathered block in sparse steps
+  const int kv_box = (s.bn == 32) ? (sparse ? 32 : 128) : s.bn;
   int st = encode_map(&maps[0], q, rows, s.d, 128);
-  if (st == WISE_OK) st = encode_map(&maps[1], k, kv_rows, s.d, s.bn);
-  if (st == WISE_OK) st = encode_map(&maps[2], v, kv_rows, s.d, s.bn);
+  if (st == WISE_OK) st = encode_map(&maps[1], k, kv_rows, s.d, kv_box);
+  if (st == WISE_OK) st = encode_map(&maps[2], v, kv_rows, s.d, kv_box);
   if (st != WISE_OK) return st;
   AttnParams p;
   memset(&p, 0, sizeof(p));

@@ -37,7 +37,9 @@
  * - Masking is causal: key j is admissible for query i iff j <= i; key block
  *   b is admissible for query block q iff b <= q. One call is one attention
  *   layer.
- * - Supported shapes: head_dim in {64, 96, 128}; block in {64, 128};
+ * - Supported shapes: head_dim in {64, 96, 128}; block in {32, 64, 128}
+ *   (32 is the pages' default support granularity; the kernels work on
+ *   128-row query tiles, i.e. four query blocks of 32 share one tile);
  *   seq_len a positive multiple of block with seq_len / block <= 1024;
  *   batch * heads >= 1. Base pointers of Q/K/V/O must be 16-byte aligned.
  * - The library never allocates or frees memory and keeps no state besides

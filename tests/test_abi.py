@@ -75,10 +75,23 @@ def test_invalid_descriptor_rejected(lib, bad):
     assert st == _lib.WISE_ERR_INVALID_ARGUMENT
 
 
-@pytest.mark.parametrize("bad", [dict(d=80), dict(d=256), dict(blk=32), dict(blk=256), dict(n=64 * 2048)])
+@pytest.mark.parametrize("bad", [dict(d=80), dict(d=256), dict(blk=16), dict(blk=256), dict(n=64 * 2048),
+                                 dict(blk=32, n=32 * 1056)])
 def test_unsupported_shapes_rejected(lib, bad):
     d = _desc(**bad)
     assert lib.wise_attn_discover(d, 16, 16, 16, 16, None, None, None, 0, None) == _lib.WISE_ERR_UNSUPPORTED
+
+
+def test_block_32_queries(lib):
+    # blocks of 32 (the pages' default granularity): four query blocks per
+    # 128-row tile; the Eq 5 scratch holds four values per row and 128-key span
+    n = 640
+    d = _desc(2, 3, n, 64, 32)
+    nb, tiles = n // 32, (n + 127) // 128
+    assert lib.wise_support_capacity(d) == 2 * 3 * nb * (nb + 1) // 2
+    assert lib.wise_schedule_units(d) == 2 * 3 * tiles
+    assert lib.wise_attn_discover_workspace(d) == 2 * 3 * 4 * tiles * (tiles + 1) // 2 * 128 * 4
+    assert lib.wise_select_workspace(d, 3) > 0
 
 
 def test_null_and_misaligned_pointers_rejected(lib):

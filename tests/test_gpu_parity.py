@@ -455,3 +455,165 @@ def test_static95_is_a_one_step_window():
     for hi in range(h):
         want += [sorted(O.step_support(m[0, 0, hi, q].astype(np.float64), q, 0.95)) for q in range(nb)]
     assert sup.to_lists() == want
+
+
+# ------------------------- blocks of 32 (the pages' default granularity) ----
+# Discovery runs on contiguous 128-key spans with one Eq 5 partial sum per
+# 32-key block; sparse steps gather any four 32-key blocks listed by the
+# tile's four query blocks into one 128-key entry with a per-(query block,
+# slot) mask.
+
+B32_SHAPES = [  # (batch, heads, n, d)
+    (1, 2, 256, 64),
+    (1, 1, 32, 64),       # one block in one partial tile
+    (1, 1, 96, 128),      # three query blocks in one partial tile
+    (2, 1, 480, 96),      # ragged last tile: three of its four query blocks exist
+    (1, 2, 1024, 128),
+    (1, 1, 2048, 64),     # lists longer than 32 entries
+]
+
+
+@pytest.mark.parametrize("shape", B32_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_block32_discover_parity(shape):
+    b, h, n, d = shape
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=n + d + 32, scale=1.5, planted=2)
+    o, lse, mass = wise.discover(q, k, v, 32, out_dtype=torch.float32)
+    wise.check_device()
+    o_ref, lse_ref, r_ref = _oracle_discover(x, 32)
+    _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
+    _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+    _assert_close("mass", mass.cpu().numpy(), r_ref, MASS_TOL)
+    iu = np.triu_indices(n // 32, 1)
+    assert np.all(mass.cpu().numpy()[..., iu[0], iu[1]] == 0.0)
+
+
+def _sparse_vs_oracle(x, q, k, v, rows, b, h, n, d, blk=32, use_schedule=False):
+    sup = wise.support_from_lists(rows, b, h, n, d, blk)
+    o, lse = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=use_schedule)
+    wise.check_device()
+    rp, ci = O.support_to_csr(rows)
+    o_ref, lse_ref = O.sparse(x[0].astype(np.float64), x[1].astype(np.float64), x[2].astype(np.float64), blk, rp, ci)
+    _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
+    _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+    return o, lse
+
+
+@pytest.mark.parametrize("shape", B32_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("density", [0.1, 0.5])
+def test_block32_sparse_parity_random_support(shape, density):
+    b, h, n, d = shape
+    nb = n // 32
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=5 * n + d, scale=1.5, planted=2)
+    rng = np.random.default_rng(n + 32)
+    rows = []
+    for _ in range(b * h):
+        rows.extend(wl.random_support(nb, density, rng, sink=bool(rng.integers(0, 2)), diag=bool(rng.integers(0, 2))))
+    _sparse_vs_oracle(x, q, k, v, rows, b, h, n, d)
+
+
+def test_block32_sparse_structured_supports():
+    b, h, n, d = 1, 1, 1024, 128
+    nb = n // 32
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=17, scale=1.5, planted=2)
+    # sink and diagonal only: each tile gathers block 0 and its four diagonal blocks
+    _sparse_vs_oracle(x, q, k, v, [sorted({0, qb}) for qb in range(nb)], b, h, n, d)
+    # one shared column plus the diagonal
+    _sparse_vs_oracle(x, q, k, v, [sorted({min(5, qb), qb}) for qb in range(nb)], b, h, n, d)
+    # the four query blocks of a tile list disjoint blocks
+    rows = [[kb for kb in range(qb + 1) if kb % 4 == qb % 4] for qb in range(nb)]
+    _sparse_vs_oracle(x, q, k, v, rows, b, h, n, d)
+    # only the diagonal block (causal inside the block only)
+    _sparse_vs_oracle(x, q, k, v, [[qb] for qb in range(nb)], b, h, n, d)
+
+
+def test_block32_sparse_full_support_bitwise_equals_discover():
+    b, h, n, d = 1, 2, 768, 128
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=13, scale=1.5, planted=2)
+    nb = n // 32
+    rows = [list(range(qb + 1)) for _ in range(b * h) for qb in range(nb)]
+    sup = wise.support_from_lists(rows, b, h, n, d, 32)
+    o1, l1 = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    o2, l2, _ = wise.discover(q, k, v, 32, want_mass=False, out_dtype=torch.float32)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_block32_sparse_empty_rows_and_tiles():
+    b, h, n, d = 1, 1, 512, 64
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=6)
+    nb = n // 32
+    rows = [[0] if qb % 3 == 0 else [] for qb in range(nb)]
+    for qb in range(4, 8):  # a whole tile with no entries
+        rows[qb] = []
+    o, lse = _sparse_vs_oracle(x, q, k, v, rows, b, h, n, d)
+    on, ln = o.cpu().numpy(), lse.cpu().numpy()
+    assert np.all(on[0, 0, 128:256] == 0) and np.all(np.isneginf(ln[0, 0, 128:256]))
+    assert np.all(on[0, 0, 32:64] == 0) and np.all(np.isneginf(ln[0, 0, 32:64]))
+
+
+def test_block32_sparse_malformed_support_is_flagged_not_faulted():
+    b, h, n, d = 1, 1, 256, 64
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=8)
+    rows = [[0], [1, 0], [0, 7, 2], [-3, 3], [0, 4], [5, 5], [2], [1 << 20]]
+    sup = wise.support_from_lists(rows, b, h, n, d, 32)
+    wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    assert wise.device_status() == wise._lib.WISE_ERR_BAD_SUPPORT
+    assert wise.device_status() == wise._lib.WISE_OK
+
+
+@pytest.mark.parametrize("case", [(2, 1, 2, 40, 0.9), (3, 2, 1, 128, 0.95), (1, 1, 1, 1024, 0.8), (2, 1, 3, 7, 0.9)],
+                         ids=lambda c: "W%d_B%d_H%d_nb%d_eta%s" % c)
+@pytest.mark.parametrize("flags", [0, 3])
+def test_block32_select_bit_exact_on_same_masses(case, flags):
+    w, b, h, nb, eta = case
+    m = _random_masses(w, b, h, nb, seed=nb * 11 + w, ties=True)
+    sup = wise.select_support(torch.from_numpy(m).cuda(), nb * 32, 64, 32, eta, flags)
+    wise.check_device()
+    rp_ref, ci_ref = O.select(m.astype(np.float64), eta, flags)
+    rp = sup.row_ptr.cpu().numpy()
+    assert np.array_equal(rp, rp_ref)
+    assert np.array_equal(sup.col_idx.cpu().numpy()[:rp[-1]], ci_ref)
+    _check_tile_order(sup)
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 2, 384, 128), (2, 4, 1, 224, 64), (1, 6, 3, 512, 96)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_block32_grouped_query(shape):
+    b, h, hk, n, d = shape
+    x, q, k, v = _gqa_inputs(b, h, hk, n, d, seed=n + h + hk + 32)
+    o, lse, mass = wise.discover(q, k, v, 32, out_dtype=torch.float32)
+    wise.check_device()
+    o_ref, lse_ref, r_ref = _oracle_discover(x, 32)
+    _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
+    _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+    _assert_close("mass", mass.cpu().numpy(), r_ref, MASS_TOL)
+    rng = np.random.default_rng(h * n + 32)
+    rows = [r for _ in range(b * h) for r in wl.random_support(n // 32, 0.3, rng)]
+    _sparse_vs_oracle(x, q, k, v, rows, b, h, n, d)
+
+
+def test_block32_trajectory_end_to_end():
+    cfg = wl.CONFIGS["tiny"].replace(name="tiny_b32", seq_len=512, block=32)
+    sup, outs = _run_trajectory(cfg)
+    rows = sup.to_lists()
+    nb = cfg.n_blocks
+    for bi in range(cfg.batch):
+        for hi in range(cfg.heads):
+            om = []
+            for t in cfg.window_steps:
+                x = outs[t][0]
+                _, _, r = O.causal_attention(*(x[i, bi, hi].astype(np.float64) for i in range(3)), cfg.block,
+                                             want_mass=True)
+                om.append(r)
+                _assert_close("mass", outs[t][3][bi, hi], r, MASS_TOL)
+            base = (bi * cfg.heads + hi) * nb
+            _assert_support_matches(rows[base:base + nb], om, cfg, rows[base:base + nb])
+    rp = sup.row_ptr.cpu().numpy()
+    ci = sup.col_idx.cpu().numpy()
+    for t in range(cfg.t_d, cfg.steps):
+        x = wl.step_inputs(cfg, t)
+        q, k, v = (torch.from_numpy(x[i]).to(torch.bfloat16).cuda() for i in range(3))
+        o, lse = wise.sparse(q, k, v, sup, out_dtype=torch.float32)
+        o_ref, lse_ref = O.sparse(x[0].astype(np.float64), x[1].astype(np.float64), x[2].astype(np.float64),
+                                  cfg.block, rp, ci)
+        _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
+        _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)

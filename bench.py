@@ -59,6 +59,30 @@ def support_flops(row_ptr: np.ndarray, col_idx: np.ndarray, nb: int, block: int,
     return 4.0 * head_dim * (off * block * block + diag * block * (block + 1) / 2)
 
 
+def tile_entries(row_ptr: np.ndarray, col_idx: np.ndarray, bh: int, nb: int, block: int) -> int:
+    """Entries (K/V tiles) one sparse step runs: per 128-row query tile, the
+    distinct key blocks its query blocks list; blocks of 32 are gathered four
+    to an entry."""
+    per_tile = 128 // block
+    tiles = -(-nb // per_tile)
+    listed = np.zeros((bh, tiles * per_tile, nb), dtype=bool)
+    rows = np.repeat(np.arange(bh * nb), np.diff(row_ptr))
+    cols = col_idx[:row_ptr[-1]]
+    listed[rows // nb, rows % nb, cols] = True
+    union = listed.reshape(bh, tiles, per_tile, nb).any(axis=2).sum(axis=2)
+    if block == 32:
+        union = -(-union // 4)
+    return int(union.sum())
+
+
+def tile_flops(entries: int, block: int, head_dim: int) -> float:
+    """FLOPs the tensor core executes for `entries` tiles: S = Q K^T and
+    O += P V over 128 query rows and one entry's keys (128, or 64 for blocks
+    of 64)."""
+    keys = 64 if block == 64 else 128
+    return 4.0 * head_dim * 128 * keys * entries
+
+
 def reduce_max_over_ranks(values, world, device=None):
     """Element-wise max over ranks (the slowest rank sets the time)."""
     import torch
@@ -155,13 +179,33 @@ def stored_traffic(kernel: str, workload: str):
 
 # --------------------------------------------------------------------------- GPU arm
 
+def workload(args):
+    """The configuration's workload, with the support block size replaced
+    when --block asks for another one (the generator plants its evidence in
+    blocks of that size)."""
+    cfg = wl.CONFIGS[args.config]
+    if args.block and args.block != cfg.block:
+        cfg = cfg.replace(block=args.block)
+    return cfg
+
+
+def workload_name(args, cfg) -> str:
+    base = wl.CONFIGS[args.config]
+    return f"wise_{cfg.name}" + (f"_b{cfg.block}" if cfg.block != base.block else "")
+
+
+def traffic_key(args) -> str:
+    base = wl.CONFIGS[args.config]
+    return args.config if not args.block or args.block == base.block else f"{args.config}_b{args.block}"
+
+
 def run_gpu(args, rank, world):
     import torch
     import block_sparse_attention_causal_gb300 as wise
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    cfg = wl.CONFIGS[args.config]
+    cfg = workload(args)
     B, H, n, d, blk = cfg.batch, cfg.heads, cfg.seq_len, cfg.head_dim, cfg.block
     nb = cfg.n_blocks
     T, td, W = cfg.steps, cfg.t_d, cfg.window
@@ -256,6 +300,8 @@ def run_gpu(args, rank, world):
     rp = support.row_ptr.cpu().numpy()
     ci = support.col_idx.cpu().numpy()
     sparse_flops = support_flops(rp, ci, nb, blk, d)
+    entries = tile_entries(rp, ci, B * H, nb, blk)
+    sparse_tile_flops = tile_flops(entries, blk, d)
     dense_flops = wise.dense_flops(B, H, n, d)
     density = float(rp[-1]) / (B * H * nb * (nb + 1) / 2)
 
@@ -313,6 +359,7 @@ def run_gpu(args, rank, world):
             kern_stats[k_]["tflops"] = dense_flops / (kern_stats[k_]["avg_ms"] * 1e-3) / 1e12
     if "sparse" in kern_stats:
         kern_stats["sparse"]["tflops"] = sparse_flops / (kern_stats["sparse"]["avg_ms"] * 1e-3) / 1e12
+        kern_stats["sparse"]["tile_tflops"] = sparse_tile_flops / (kern_stats["sparse"]["avg_ms"] * 1e-3) / 1e12
     if "select" in kern_stats:
         sel_bytes = W * B * H * nb * nb * 4 + (B * H * nb + 1) * 4 + rp[-1] * 4
         kern_stats["select"]["gbs"] = sel_bytes / (kern_stats["select"]["avg_ms"] * 1e-3) / 1e9
@@ -323,18 +370,18 @@ def run_gpu(args, rank, world):
                    "discover_mass": "wise_attn_kernel<dense,mass>"}[dominant]
     roofline = {"kernel": kernel_name, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
-                "traffic": stored_traffic(dominant, args.config),
+                "traffic": stored_traffic(dominant, traffic_key(args)),
                 "peak_source": f"bf16_tflops ({peak_kind}, burst)",
                 "algorithmic": "4*d FLOPs per admissible query-key pair inside the support"}
     sparse_roof = {"achieved": round(kern_stats["sparse"]["tflops"], 2), "peak": peak_tf,
                    "frac": round(kern_stats["sparse"]["tflops"] / peak_tf, 4),
-                   "traffic": stored_traffic("sparse", args.config)}
+                   "traffic": stored_traffic("sparse", traffic_key(args))}
 
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(traj_ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"wise_{cfg.name}", "batch": B, "heads": H, "seq_len": n, "head_dim": d,
+        "config": {"workload": workload_name(args, cfg), "batch": B, "heads": H, "seq_len": n, "head_dim": d,
                    "block": blk, "steps_T": T, "t_d": td, "window": W, "eta": cfg.eta,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "each trajectory reads T distinct step inputs "
@@ -344,6 +391,7 @@ def run_gpu(args, rank, world):
         "dense_tflops": round(dense_tflops, 2), "frac_of_bf16_peak": round(value / world / peak_tf, 4),
         "support_density": round(density, 4), "nnz": int(rp[-1]),
         "sparse_useful_tflop_per_step": sparse_flops / 1e12, "dense_tflop_per_step": dense_flops / 1e12,
+        "sparse_tile_entries": entries, "sparse_tile_tflop_per_step": sparse_tile_flops / 1e12,
         "setup_inclusive_speedup": round((n_late * dense_ms) /
                                          (kern_stats["select"]["avg_ms"] + n_late * sparse_ms), 3),
         "trajectory_speedup": round(T * dense_ms / traj_ms, 3),
@@ -458,7 +506,7 @@ def cpu_baseline(cfg, seed, rows_by_head, budget_s: float = 10.0):
 def run_reference(args, rank, world):
     """The oracle arm: per step, one head's late step through the fp64 oracle
     over the support the oracle itself selects (selection untimed)."""
-    cfg = wl.CONFIGS[args.config]
+    cfg = workload(args)
     rows = _oracle_rows(cfg, args.seed, 0, 0)
     for _ in range(args.warmup):
         _oracle_late_step(cfg, args.seed, 0, 0, rows)
@@ -474,7 +522,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / max(1, args.steps) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"wise_{cfg.name}", "batch": cfg.batch, "heads": cfg.heads,
+        "config": {"workload": workload_name(args, cfg), "batch": cfg.batch, "heads": cfg.heads,
                    "seq_len": cfg.seq_len, "head_dim": cfg.head_dim, "block": cfg.block},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"per step: the late step (Eq 8) of one (batch, head) slice of {cfg.name} over "
@@ -492,6 +540,8 @@ def main():
     ap.add_argument("--impl", default="wise", choices=["wise", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--block", type=int, default=0, choices=[0, 32, 64, 128],
+                    help="support block size (0: the configuration's own)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "wise" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))

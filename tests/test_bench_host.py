@@ -26,6 +26,26 @@ def test_support_flops_counts_admissible_pairs():
     assert bench.support_flops(rp, ci, 3, blk, d) == 4.0 * d * brute
 
 
+def test_tile_entries_count_what_the_scheduler_forms():
+    # one head, nb = 6 blocks of 32: two 128-row tiles, the second ragged
+    # (query blocks 4 and 5 only). Tile 0's rows list {0, 1, 2, 3}: one
+    # gathered entry; tile 1's list {0, 4, 5}: one.
+    rows = [[0], [0, 1], [1, 2], [0, 3], [0, 4], [4, 5]]
+    rp = np.cumsum([0] + [len(r) for r in rows]).astype(np.int32)
+    ci = np.array(sum(rows, []), np.int32)
+    assert bench.tile_entries(rp, ci, 1, 6, 32) == 2
+    # six distinct blocks in tile 1 need two entries
+    rows2 = [[0], [0, 1], [1, 2], [0, 2, 3], [0, 1, 2, 4], [3, 5]]
+    rp2 = np.cumsum([0] + [len(r) for r in rows2]).astype(np.int32)
+    ci2 = np.array(sum(rows2, []), np.int32)
+    assert bench.tile_entries(rp2, ci2, 1, 6, 32) == 1 + 2
+    # blocks of 64: the union of two rows per tile ({0,1}, {0,1,2,3}, {0,4,5});
+    # of 128: every listed block
+    assert bench.tile_entries(rp, ci, 1, 6, 64) == 2 + 4 + 3
+    assert bench.tile_entries(rp, ci, 1, 6, 128) == len(ci)
+    assert bench.tile_flops(3, 64, 128) == 4.0 * 128 * 128 * 64 * 3
+
+
 def test_whole_job_value_is_weak_scaling():
     assert bench.whole_job_tflops(2e12, 1000.0, 1) == pytest.approx(2.0)
     assert bench.whole_job_tflops(2e12, 1000.0, 4) == pytest.approx(8.0)

@@ -29,7 +29,7 @@ cudaError_t launch_one(const CUtensorMap* m, const AttnParams& p, cudaStream_t s
   AttnParams q = p;
   q.sched_slot = launches.fetch_add(1u) % kSchedSlots;
   const int64_t grid = p.n_units < sm_count[dev] ? p.n_units : sm_count[dev];
-  wise_attn_kernel<D, BN, SPARSE><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(m[0], m[1], m[2], q);
+  wise_attn_kernel<D, BN, SPARSE><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(m[0], m[1], m[2], m[3], m[4], q);
   return cudaGetLastError();
 }
 
@@ -37,7 +37,10 @@ cudaError_t launch_one(const CUtensorMap* m, const AttnParams& p, cudaStream_t s
 
 cudaError_t launch_attn_d96(int block, bool sparse, const CUtensorMap* maps, const AttnParams& p, cudaStream_t st) {
   if (block == 128) return sparse ? launch_one<96, 128, true>(maps, p, st) : launch_one<96, 128, false>(maps, p, st);
-  if (block == 32) return sparse ? launch_one<96, 32, true>(maps, p, st) : launch_one<96, 32, false>(maps, p, st);
+  // blocks of 32: discovery without masses is the dense kernel of blocks of 128
+  if (block == 32)
+    return sparse ? launch_one<96, 32, true>(maps, p, st)
+                  : (p.mass ? launch_one<96, 32, false>(maps, p, st) : launch_one<96, 128, false>(maps, p, st));
   return sparse ? launch_one<96, 64, true>(maps, p, st) : launch_one<96, 64, false>(maps, p, st);
 }
 

@@ -535,14 +535,24 @@ __device__ __forceinline__ void gather_scheduler(const AttnParams& p, const CUte
 }
 
 // TMA loads of one K or V tile (KV_BYTES, announced on `bar` by the caller):
-// one box per 64 (or 32) columns of the head dimension; for gathered entries,
-// four 32-row boxes per column chunk, one per slot, at the slot's key block.
+// one box per 64 (or 32) columns of the head dimension (map `tm`); for
+// gathered entries, four 32-row boxes per column chunk (map `tm`), one per
+// slot at the slot's key block, or one 128-row box (map `tm4`) when the four
+// blocks are consecutive.
 template <class C>
-__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar, const EntryRec& e) {
+__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* tm, const CUtensorMap* tm4,
+                                             uint64_t* bar, const EntryRec& e) {
   for (int c = 0; c < C::NCH; ++c) tma_load_2d(dst + c * C::KW * C::ROWB, tm, bar, c * C::CH, (int)e.krow);
 }
 template <class C>
-__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar, const GatherRec& e) {
+__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* tm, const CUtensorMap* tm4,
+                                             uint64_t* bar, const GatherRec& e) {
+  const int kb0 = gather_kb(e, 0);
+  if (gather_kb(e, 1) == kb0 + 1 && gather_kb(e, 2) == kb0 + 2 && gather_kb(e, 3) == kb0 + 3) {
+    for (int c = 0; c < C::NCH; ++c)
+      tma_load_2d(dst + c * C::KW * C::ROWB, tm4, bar, c * C::CH, (int)e.kvrow0 + 32 * kb0);
+    return;
+  }
 #pragma unroll
   for (int sl = 0; sl < 4; ++sl) {
     const int row = (int)e.kvrow0 + 32 * gather_kb(e, sl);
@@ -553,7 +563,8 @@ __device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* tm
 template <int D, int BN, bool SPARSE>
 __global__ void __launch_bounds__(512, 1)
     wise_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k4,
+                     const __grid_constant__ CUtensorMap tm_v4, const AttnParams p) {
   using C = AttnCfg<D, BN, SPARSE>;
   constexpr int NK = C::NK, NV = C::NV, META = C::META;
   constexpr uint32_t ROWB = C::ROWB;
@@ -769,6 +780,10 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      if (C::GATHER) {
+        tma_prefetch_desc(&tm_k4);
+        tma_prefetch_desc(&tm_v4);
+      }
     }
     uint32_t nq0 = 0u, nq1 = 0u;  // Q loads per stream
     uint32_t rk = 0, rv = 0;    // next record for K / V
@@ -812,7 +827,7 @@ __global__ void __launch_bounds__(512, 1)
         uint8_t* dst = smem + C::OFF_K + slot * C::KV_BYTES;
         if (leader) {
           mbar_arrive_expect_tx(&k_full[slot], C::KV_BYTES);
-          load_kv_tile<C>(dst, &tm_k, &k_full[slot], e);
+          load_kv_tile<C>(dst, &tm_k, &tm_k4, &k_full[slot], e);
         }
         ++nk;
       } else {
@@ -828,7 +843,7 @@ __global__ void __launch_bounds__(512, 1)
         uint8_t* dst = smem + C::OFF_V + slot * C::KV_BYTES;
         if (leader) {
           mbar_arrive_expect_tx(&v_full[slot], C::KV_BYTES);
-          load_kv_tile<C>(dst, &tm_v, &v_full[slot], e);
+          load_kv_tile<C>(dst, &tm_v, &tm_v4, &v_full[slot], e);
         }
         ++nv;
       }
@@ -988,10 +1003,11 @@ __global__ void __launch_bounds__(512, 1)
     const bool want_mass = (!SPARSE) && (p.mass != nullptr);
     const int half = (BN == 64) ? (r >> 6) : 0;
     constexpr int NC = C::KW / 32;  // 32-column chunks of a score row
-    // blocks of 32: the fp32 row sum is taken per 32-column chunk (one Eq 5
-    // partial sum per key block in discovery); sparse steps add in the same
-    // order, so a full support reproduces discovery bit for bit
-    constexpr bool CHUNK_SUMS = (BN == 32);
+    // blocks of 32 in discovery: the fp32 row sum is taken per 32-column
+    // chunk (one Eq 5 partial sum per key block). Only discovery with masses
+    // runs this variant: without masses, blocks of 32 use the kernel for
+    // blocks of 128 (the same arithmetic as gathered sparse steps).
+    constexpr bool CHUNK_SUMS = (BN == 32) && !SPARSE;
     float* st = stats + s * C::ST_STRIDE;
     float m_ref = -INFINITY, l = 0.f, lt = 0.f;
     uint32_t cnt = 0, ne = 0, nst = 0;

@@ -50,7 +50,8 @@ struct SelectLaunch {
 };
 
 // Launch the attention kernel for one head dimension (defined in
-// attn_d{64,96,128}.cu). maps = {Q, K, V} tensor maps.
+// attn_d{64,96,128}.cu). maps = {Q, K, V, K128, V128} tensor maps (the last
+// two with 128-row boxes, for consecutive gathered blocks of 32).
 cudaError_t launch_attn_d64(int block, bool sparse, const CUtensorMap* maps, const AttnParams& p, cudaStream_t st);
 cudaError_t launch_attn_d96(int block, bool sparse, const CUtensorMap* maps, const AttnParams& p, cudaStream_t st);
 cudaError_t launch_attn_d128(int block, bool sparse, const CUtensorMap* maps, const AttnParams& p, cudaStream_t st);

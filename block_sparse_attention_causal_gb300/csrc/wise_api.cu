@@ -132,7 +132,9 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
   const Shape s = shape_of(desc);
   uint32_t* err = error_word();
   if (!err) return WISE_ERR_CUDA;
-  CUtensorMap maps[3];
+  // Q, K, V, and K, V with 128-row boxes (consecutive gathered blocks; the
+  // same maps as K, V for the other variants)
+  CUtensorMap maps[5];
   const int64_t rows = s.bh * s.n;
   const int64_t kv_rows = (int64_t)desc->batch * s.kv_heads * s.n;
   // K/V boxes: one key block (64 or 128 rows); blocks of 32 use 128-row
@@ -141,6 +143,8 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
   int st = encode_map(&maps[0], q, rows, s.d, 128);
   if (st == WISE_OK) st = encode_map(&maps[1], k, kv_rows, s.d, kv_box);
   if (st == WISE_OK) st = encode_map(&maps[2], v, kv_rows, s.d, kv_box);
+  if (st == WISE_OK) st = encode_map(&maps[3], k, kv_rows, s.d, kv_box == 32 ? 128 : kv_box);
+  if (st == WISE_OK) st = encode_map(&maps[4], v, kv_rows, s.d, kv_box == 32 ? 128 : kv_box);
   if (st != WISE_OK) return st;
   AttnParams p;
   memset(&p, 0, sizeof(p));

@@ -231,7 +231,11 @@ def run_gpu(args, rank, world):
     sel_ws = torch.empty(max(16, int(lib.wise_select_workspace(desc, W))), dtype=torch.uint8, device=dev)
     support = wise.select_support(torch.zeros_like(masses), n, d, blk, cfg.eta, workspace=sel_ws)
 
-    names = ["discover_mass", "discover", "select", "sparse"]
+    # selection fused into the window's discovery launches (nb <= 256), or
+    # one selection pass over the window's masses
+    fused = args.selection == "fused" and nb <= 256
+    sel_state = wise.new_select_state((B, H, n, d), blk, W) if fused else None
+    names = ["discover_mass", "discover_select", "discover", "select", "sparse"]
     ev = {k: [] for k in names}
 
     def call(kind, fn, record):
@@ -253,16 +257,23 @@ def run_gpu(args, rank, world):
             q, k, v = inputs[t][0], inputs[t][1], inputs[t][2]
             if t < td:
                 w = t - (td - W)
-                if w >= 0:
+                if w >= 0 and fused:
+                    call("discover_select", lambda: wise.discover_select(
+                        q, k, v, blk, step=w, window=W, eta=cfg.eta, select_state=sel_state, out=o, lse=lse,
+                        mass=masses[w], workspace=ws), record)
+                elif w >= 0:
                     call("discover_mass", lambda: wise.discover(q, k, v, blk, out=o, lse=lse, mass=masses[w],
                                                                workspace=ws), record)
                 else:
                     call("discover", lambda: wise.discover(q, k, v, blk, want_mass=False, out=o, lse=lse), record)
                 launches += 1
-                if t == td - 1:
+                if t == td - 1 and fused:
+                    call("select", lambda: wise.select_finalize(sel_state, B, H, n, d, blk, support=support), record)
+                    launches += 1
+                elif t == td - 1:
                     call("select", lambda: wise.select_support(masses, n, d, blk, cfg.eta, support=support,
                                                                workspace=sel_ws), record)
-                    launches += 4
+                    launches += 2
             else:
                 call("sparse", lambda: wise.sparse(q, k, v, support, out=o, lse=lse), record)
                 launches += 1
@@ -354,20 +365,24 @@ def run_gpu(args, rank, world):
             kern_stats[k_] = {"launches": len(vals_), "avg_ms": sum(vals_) / len(vals_),
                               "total_ms_per_step": sum(vals_) / args.steps}
     dense_tflops = dense_flops / (dense_ms * 1e-3) / 1e12
-    for k_ in ("discover", "discover_mass"):
+    for k_ in ("discover", "discover_mass", "discover_select"):
         if k_ in kern_stats:
             kern_stats[k_]["tflops"] = dense_flops / (kern_stats[k_]["avg_ms"] * 1e-3) / 1e12
     if "sparse" in kern_stats:
         kern_stats["sparse"]["tflops"] = sparse_flops / (kern_stats["sparse"]["avg_ms"] * 1e-3) / 1e12
         kern_stats["sparse"]["tile_tflops"] = sparse_tile_flops / (kern_stats["sparse"]["avg_ms"] * 1e-3) / 1e12
     if "select" in kern_stats:
-        sel_bytes = W * B * H * nb * nb * 4 + (B * H * nb + 1) * 4 + rp[-1] * 4
+        # read: the window's masses (separate pass) or the row bitmasks and
+        # counts (fused); written: the CSR
+        read = (B * H * nb * (-(-nb // 32)) * 4 + B * H * nb * 4) if fused else W * B * H * nb * nb * 4
+        sel_bytes = read + (B * H * nb + 1) * 4 + rp[-1] * 4
         kern_stats["select"]["gbs"] = sel_bytes / (kern_stats["select"]["avg_ms"] * 1e-3) / 1e9
     dominant = max((k_ for k_ in kern_stats if k_ != "select"), key=lambda k_: kern_stats[k_]["total_ms_per_step"])
     dom = kern_stats[dominant]
     achieved = dom["tflops"]
     kernel_name = {"sparse": "wise_attn_kernel<sparse>", "discover": "wise_attn_kernel<dense>",
-                   "discover_mass": "wise_attn_kernel<dense,mass>"}[dominant]
+                   "discover_mass": "wise_attn_kernel<dense,mass>",
+                   "discover_select": "wise_attn_kernel<dense,mass,select>"}[dominant]
     roofline = {"kernel": kernel_name, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
                 "traffic": stored_traffic(dominant, traffic_key(args)),
@@ -383,6 +398,7 @@ def run_gpu(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_name(args, cfg), "batch": B, "heads": H, "seq_len": n, "head_dim": d,
                    "block": blk, "steps_T": T, "t_d": td, "window": W, "eta": cfg.eta,
+                   "selection": "fused into discovery" if fused else "separate pass",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "each trajectory reads T distinct step inputs "
                          f"({T * 3 * B * H * n * d * 2 / 1e9:.2f} GB > 129 MB L2)"},
@@ -540,6 +556,8 @@ def main():
     ap.add_argument("--impl", default="wise", choices=["wise", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--selection", default="separate", choices=["fused", "separate"],
+                    help="Eq 6 selection fused into the window's discovery launches, or a separate pass")
     ap.add_argument("--block", type=int, default=0, choices=[0, 32, 64, 128],
                     help="support block size (0: the configuration's own)")
     args = ap.parse_args()

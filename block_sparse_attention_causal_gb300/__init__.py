@@ -9,7 +9,10 @@ Language Models" (WISE):
 * :func:`select_support`  -- once after discovery: the cumulative-mass block
   support of §5.1 Eq 6, unioned over the discovery window, as a CSR;
 * :func:`sparse`          -- late recurrent step: attention over the reused
-  support only (§5.2 Eqs 7-8).
+  support only (§5.2 Eqs 7-8);
+* :func:`discover_select` / :func:`select_finalize` -- the same discovery and
+  selection with each window step's Eq 6 support taken in the discovery
+  launch itself (no mass tensors kept across the window, no selection pass).
 
 Torch tensors supply device memory and the stream; every computation runs in
 the library's CUDA kernels. There is no CPU path: without the compiled
@@ -26,7 +29,8 @@ import torch
 from . import _lib
 from ._lib import (WISE_BF16, WISE_F32, WISE_SUPPORT_DIAG, WISE_SUPPORT_SINK, WiseError)  # noqa: F401
 
-__all__ = ["discover", "select_support", "sparse", "Support", "device_status", "WiseError",
+__all__ = ["discover", "select_support", "sparse", "Support", "device_status", "WiseError", "discover_select",
+           "select_finalize", "new_select_state",
            "WISE_SUPPORT_SINK", "WISE_SUPPORT_DIAG", "useful_flops", "dense_flops", "retained_mass",
            "support_jaccard", "select_control"]
 
@@ -101,6 +105,49 @@ def discover(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: int, *, w
                                 workspace.numel() if (want_mass and workspace is not None) else 0,
                                 _stream_handle(stream))
     _lib.check(st, "wise_attn_discover")
+    return out, (lse if want_lse else None), mass
+
+
+def new_select_state(shape: Sequence[int], block: int, window: int, device="cuda") -> torch.Tensor:
+    """Device buffer that carries the working set across the discovery steps
+    of one selection window (see :func:`discover_select`)."""
+    b, h, n, d = shape
+    nbytes = int(_lib.load().wise_select_workspace(_lib.make_desc(b, h, n, d, block), window))
+    if nbytes <= 0:
+        raise ValueError("unsupported shape or window")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def discover_select(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: int, *, step: int, window: int,
+                    eta: float, select_state: torch.Tensor, flags: int = WISE_SUPPORT_SINK | WISE_SUPPORT_DIAG,
+                    want_lse: bool = True, out_dtype: torch.dtype = torch.bfloat16, scale: float = 0.0,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    mass: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None):
+    """Discovery step `step` (0-based) of a selection window of `window`
+    steps, with the step's Eq 6 support OR-ed into `select_state` in the same
+    launch (WISE §5.1 Eq 6, streamed over the window). Returns (O, LSE or
+    None, this step's block masses). After the last step,
+    :func:`select_finalize` gives the Support."""
+    hk = _check_qkv(q, k, v)
+    lib = _lib.load()
+    b, h, n, d = q.shape
+    desc = _desc(q.shape, block, scale, out_dtype, hk)
+    if out is None:
+        out = torch.empty((b, h, n, d), dtype=out_dtype, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    nb = n // block
+    if mass is None:
+        mass = torch.empty((b, h, nb, nb), dtype=torch.float32, device=q.device)
+    ws_bytes = int(lib.wise_attn_discover_workspace(desc))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib.wise_attn_discover_select(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), _ptr(lse),
+                                       mass.data_ptr(), workspace.data_ptr(), workspace.numel(), float(eta), flags,
+                                       step, window, select_state.data_ptr(), select_state.numel(),
+                                       _stream_handle(stream))
+    _lib.check(st, "wise_attn_discover_select")
     return out, (lse if want_lse else None), mass
 
 
@@ -181,6 +228,29 @@ def sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, support: Support, 
                               _ptr(lse) if want_lse else None, _stream_handle(stream))
     _lib.check(st, "wise_attn_sparse")
     return out, (lse if want_lse else None)
+
+
+def select_finalize(select_state: torch.Tensor, batch: int, heads: int, seq_len: int, head_dim: int, block: int,
+                    *, support: Optional["Support"] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> "Support":
+    """The Support (CSR and work order) accumulated in `select_state` by a
+    window of :func:`discover_select` steps."""
+    lib = _lib.load()
+    desc = _lib.make_desc(batch, heads, seq_len, head_dim, block)
+    nb = seq_len // block
+    cap = int(lib.wise_support_capacity(desc))
+    units = int(lib.wise_schedule_units(desc))
+    dev = select_state.device
+    if support is None:
+        support = Support(torch.empty(batch * heads * nb + 1, dtype=torch.int32, device=dev),
+                          torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+                          torch.empty(max(units, 1), dtype=torch.int32, device=dev),
+                          torch.empty(1, dtype=torch.int32, device=dev), batch, heads, seq_len, head_dim, block)
+    st = lib.wise_select_finalize(desc, select_state.data_ptr(), select_state.numel(), support.row_ptr.data_ptr(),
+                                  support.col_idx.data_ptr(), support.col_idx.numel(),
+                                  support.tile_order.data_ptr(), support.nnz.data_ptr(), _stream_handle(stream))
+    _lib.check(st, "wise_select_finalize")
+    return support
 
 
 def support_from_lists(rows, batch: int, heads: int, seq_len: int, head_dim: int, block: int,

@@ -33,7 +33,8 @@ EXPORTS = (
     "wise_abi_version", "wise_status_str", "wise_attn_discover_workspace", "wise_attn_discover",
     "wise_schedule_units", "wise_support_capacity", "wise_select_workspace", "wise_select_support",
     "wise_attn_sparse", "wise_validate_support", "wise_device_status", "wise_select_support_noalloc",
-    "wise_support_retained_mass", "wise_support_jaccard", "wise_select_control",
+    "wise_support_retained_mass", "wise_support_jaccard", "wise_select_control", "wise_attn_discover_select",
+    "wise_select_finalize",
 )
 
 
@@ -84,6 +85,9 @@ _SIGNATURES = {
                                            _sz, _vp]),
     "wise_support_retained_mass": (ctypes.c_int, [_dp, _vp, _vp, _vp, _i64, _vp, _vp, _vp]),
     "wise_support_jaccard": (ctypes.c_int, [_dp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "wise_attn_discover_select": (ctypes.c_int, [_dp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, ctypes.c_double, _u32,
+                                                 _i32, _i32, _vp, _sz, _vp]),
+    "wise_select_finalize": (ctypes.c_int, [_dp, _vp, _sz, _vp, _vp, _i64, _vp, _vp, _vp]),
     "wise_device_status": (ctypes.c_int, [_vp]),
 }
 

@@ -43,6 +43,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "select_step.cuh"
 
 namespace wise {
 
@@ -340,6 +341,38 @@ __device__ __forceinline__ void sched_slot_done(const AttnParams& p) {
     g_sched[p.sched_slot].done = 0u;
     __threadfence();
   }
+}
+
+// Eq 6 step support of mass row (bh, q), fused into discovery: one warp,
+// the same fixed-point step as the selection kernel. The row's masses were
+// stored by this CTA's epilogue warps (read through L2 after their barrier).
+template <int NJ>
+static __device__ __noinline__ void select_row_fused(const AttnParams& p, int bh, int q, int lane) {
+  const int64_t row = (int64_t)bh * p.nb + q;
+  const float* src = p.mass + row * p.nb;
+  int64_t fx[NJ];
+#pragma unroll
+  for (int jj = 0; jj < NJ; ++jj) {
+    const int b = jj * 32 + lane;
+    fx[jj] = (b <= q) ? mass_fx(__ldcg(src + b)) : INT64_MIN;
+  }
+  uint32_t word = eq6_step_word<NJ, true>(fx, p.sel_target_fx, p.sel_tol_fx, lane);
+  uint32_t* dst = p.sel_bits + row * p.sel_nwords;
+  if (!p.sel_first && lane < p.sel_nwords) word |= __ldcg(dst + lane);  // union with the window's earlier steps
+  if (p.sel_last) {
+    // sink block 0 and diagonal block q
+    if ((p.sel_flags & 1u) && lane == 0) word |= 1u;
+    if ((p.sel_flags & 2u) && lane == (q >> 5)) word |= 1u << (q & 31);
+    const int cnt = warp_sum32(__popc(word));
+    if (lane == 0) p.sel_counts[row] = cnt;
+  }
+  if (lane < p.sel_nwords) dst[lane] = word;
+}
+static __device__ __forceinline__ void select_row_fused_any(const AttnParams& p, int bh, int q, int lane) {
+  if (p.sel_nwords <= 1) select_row_fused<1>(p, bh, q, lane);
+  else if (p.sel_nwords <= 2) select_row_fused<2>(p, bh, q, lane);
+  else if (p.sel_nwords <= 4) select_row_fused<4>(p, bh, q, lane);
+  else select_row_fused<8>(p, bh, q, lane);
 }
 
 // ------------------------------------------------ gathered entries (B = 32)
@@ -1203,6 +1236,7 @@ __global__ void __launch_bounds__(512, 1)
       float* st = stats + s * C::ST_STRIDE;
       int id = -1, cnt = 0;
       float lse2 = 0.f, inv_l = 0.f;
+      float lrow[4] = {0.f, 0.f, 0.f, 0.f};  // lse2 of rows 4 lane .. 4 lane + 3 (mass reduction)
       const uint32_t served = s ? served1 : served0;
       if (ok && !end) {
         ok = __all_sync(0xffffffffu, mbar_wait<5>(&st_full[s], served & 1, abort_flag, p.err));
@@ -1211,6 +1245,15 @@ __global__ void __launch_bounds__(512, 1)
           cnt = reinterpret_cast<const int*>(st)[257];
           lse2 = st[r];
           inv_l = st[128 + r];
+          if (want_mass && BN != 32) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) lrow[i] = st[4 * lane + i];
+          }
+          // everything the unit needs from the statistics is in registers:
+          // the stream's next unit may write them (its softmax waits for
+          // this only at its last entry)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&st_empty[s]);
           ok = __all_sync(0xffffffffu, mbar_wait<5>(&o_final[s], served & 1, abort_flag, p.err));
         }
       }
@@ -1298,9 +1341,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int row = 4 * lane + i;
-            const float v = st[row];
             // rows past n, or with no admissible key, contribute nothing
-            l2[i] = (t * 128 + row < p.n && v > -INFINITY) ? v : INFINITY;
+            l2[i] = (t * 128 + row < p.n && lrow[i] > -INFINITY) ? lrow[i] : INFINITY;
           }
 #pragma unroll 4
           for (int e = quarter; e < cnt; e += 4) {
@@ -1327,9 +1369,14 @@ __global__ void __launch_bounds__(512, 1)
           float* dst = p.mass + ((size_t)bh * p.nb + qb) * p.nb;
           for (int e = covered + r; e < p.nb; e += 128) dst[e] = 0.f;
         }
+        if (p.sel_bits != nullptr) {
+          // the unit's mass rows are complete once all four warps stored
+          // their part; warp j then selects the tile's query block j
+          named_bar_sync(3, 128);
+          const int qb = t * C::ENT_PER_TILE + quarter;
+          if (quarter < C::ENT_PER_TILE && qb < p.nb) select_row_fused_any(p, bh, qb, lane);
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&st_empty[s]);
       if (s) ++served1;
       else ++served0;
     }

@@ -27,6 +27,16 @@ struct AttnParams {
   int64_t n_units;
   uint32_t* err;
   uint32_t sched_slot;  // work-counter slot of this launch
+  // Selection fused into discovery with masses (one step of the window):
+  // each completed mass row's Eq 6 step support is written (first step) or
+  // OR-ed into sel_bits; the last step adds the sink / diagonal blocks and
+  // writes the row counts. Off when sel_bits is null.
+  uint32_t* sel_bits;   // [bh * nb, sel_nwords]
+  int32_t* sel_counts;  // [bh * nb]
+  int64_t sel_target_fx, sel_tol_fx;
+  int32_t sel_nwords;
+  int32_t sel_first, sel_last;
+  uint32_t sel_flags;
 };
 
 struct SelectLaunch {
@@ -43,6 +53,7 @@ struct SelectLaunch {
   int32_t* tile_order;
   int32_t units_per_bh, qb_per_unit, group_heads;
   int32_t mode;                // 0: Eq 6; 1: MassMatched; 2: SizeMatched (window 1)
+  int32_t finalize_only;       // bits and counts are already built (fused selection)
   const int32_t* ref_row_ptr;  // reference working set of the controls
   const int32_t* ref_col_idx;
   int64_t ref_cap;

@@ -4,15 +4,11 @@
 // implementation".
 //
 //  select_rows_kernel : one warp per (batch, head, query block) row. For each
-//      window step it finds the Eq 6 support without sorting: masses become
-//      int64 fixed point (2^-52 units); a bitwise search finds the largest
-//      value v* whose "mass of all blocks >= v*" still reaches eta; then
-//      k = |{> v*}| + ceil((eta - sum{> v*}) / v*) and v* is the k-th mass in
-//      (mass desc, index asc) order. Near-ties within the tolerance of v* are
-//      resolved toward lower indices with ballots in index order. Element jj
-//      of lane l is block 32*jj + l, so the ballot at step jj is word jj of
-//      the row's support bitmask (kept by lane jj). Steps are OR-ed, then the
-//      sink / diagonal blocks added.
+//      window step it finds the Eq 6 support without sorting (select_step.cuh:
+//      int64 fixed point, a search for the k-th mass, near-ties toward lower
+//      indices). Element jj of lane l is block 32*jj + l, so the ballot at
+//      step jj is word jj of the row's support bitmask (kept by lane jj).
+//      Steps are OR-ed, then the sink / diagonal blocks added.
 //      The same kernel builds the two early-static controls of WISE's
 //      Appendix B ("Intervention controls") from one step's masses and a
 //      reference working set: MassMatched (Eqs 20-21) replaces eta by the
@@ -27,6 +23,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "select_step.cuh"
 
 namespace wise {
 
@@ -55,31 +52,6 @@ struct SelectParams {
   int64_t ref_cap;
   uint32_t* err;
 };
-
-__device__ __forceinline__ int64_t warp_sum64(int64_t v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-// Warp sum of lane values in [0, 2^63 / 32): three 21-bit slices summed with
-// the hardware reduction (each slice sum < 2^26), then recombined exactly.
-__device__ __forceinline__ int64_t warp_sum_u63(int64_t v) {
-  const uint64_t u = static_cast<uint64_t>(v);
-  const uint32_t a = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(u & 0x1FFFFFu));
-  const uint32_t b = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>((u >> 21) & 0x1FFFFFu));
-  const uint32_t c = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(u >> 42));
-  return static_cast<int64_t>(a) + (static_cast<int64_t>(b) << 21) + (static_cast<int64_t>(c) << 42);
-}
-__device__ __forceinline__ int64_t warp_max64(int64_t v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = max(v, (int64_t)__shfl_xor_sync(0xffffffffu, v, off));
-  return v;
-}
-__device__ __forceinline__ int warp_sum32(int v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
 
 // 8 warps per CTA, one row per warp; NJ rounds of 32 blocks cover nb <= 32 NJ.
 template <int NJ>
@@ -123,17 +95,8 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) {
       const int b = jj * 32 + lane;  // coalesced load order: jj-major
-      fx[jj] = (b < nadm) ? __double2ll_rn((double)__ldg(src + b) * 4503599627370496.0) : INT64_MIN;
+      fx[jj] = (b < nadm) ? mass_fx(__ldg(src + b)) : INT64_MIN;
     }
-    int64_t total_pos = 0, max_pos = 0;
-#pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) {
-      total_pos += (fx[jj] > 0) ? fx[jj] : 0;
-      max_pos = max(max_pos, fx[jj]);
-    }
-    total_pos = warp_sum64(total_pos);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) max_pos = max(max_pos, (int64_t)__shfl_xor_sync(0xffffffffu, max_pos, off));
     uint32_t sel_word_mine = 0;  // the word this lane will hold (word index = lane)
     int64_t target = p.target_fx;
     if (p.mode == 1) {  // MassMatched: the mass the reference covers at this step
@@ -156,6 +119,10 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
           for (int j = 0; j < 32; ++j) c += (__shfl_sync(0xffffffffu, fx[0], j) >= fx[0]) ? 1 : 0;
           v = warp_max64((fx[0] != INT64_MIN && c >= ref_k) ? fx[0] : 0);
         } else {
+          int64_t max_pos = 0;
+#pragma unroll
+          for (int jj = 0; jj < NJ; ++jj) max_pos = max(max_pos, fx[jj]);
+          max_pos = warp_max64(max_pos);
           for (int bit = 63 - __clzll(max_pos > 0 ? max_pos : 1); bit >= 0; --bit) {
             const int64_t cand = v | (int64_t(1) << bit);
             int cnt = 0;
@@ -184,67 +151,8 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
         const uint32_t bal = __ballot_sync(0xffffffffu, pick);
         if (lane == jj) sel_word_mine = bal;
       }
-    } else if (total_pos < target) {
-      // Eq 6 cannot reach eta: every admissible block.
-#pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) {
-        const uint32_t bal = __ballot_sync(0xffffffffu, fx[jj] != INT64_MIN);
-        if (lane == jj) sel_word_mine = bal;
-      }
     } else {
-      // largest v with sum_{fx >= v} fx >= target (v > 0 since target > 0);
-      // v <= the largest mass, so bits above its top bit stay zero
-      int64_t v = 0;
-      if (NJ == 1) {
-        // one value per lane: v = the largest value x with sum{>= x} >= target
-        // (the value the bitwise search below converges to)
-        const int64_t mine = fx[0];
-        int64_t acc = 0;
-#pragma unroll 8
-        for (int j = 0; j < 32; ++j) {
-          const int64_t o = __shfl_sync(0xffffffffu, mine, j);
-          acc += (o >= mine && o > 0) ? o : 0;
-        }
-        v = warp_max64((mine > 0 && acc >= target) ? mine : 0);
-      } else {
-        for (int bit = 63 - __clzll(max_pos); bit >= 0; --bit) {
-          const int64_t cand = v | (int64_t(1) << bit);
-          int64_t sacc = 0;
-#pragma unroll
-          for (int jj = 0; jj < NJ; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
-          sacc = warp_sum_u63(sacc);
-          if (sacc >= target) v = cand;
-        }
-      }
-      int64_t s_gt = 0;
-      int c_gt = 0, c_above = 0;
-      const int64_t hi = v + p.tol_fx, lo = v - p.tol_fx;
-#pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) {
-        s_gt += (fx[jj] > v) ? fx[jj] : 0;
-        c_gt += (fx[jj] > v) ? 1 : 0;
-        c_above += (fx[jj] > hi) ? 1 : 0;
-      }
-      s_gt = warp_sum64(s_gt);
-      c_gt = warp_sum32(c_gt);
-      c_above = warp_sum32(c_above);
-      const int64_t need = target - s_gt;  // > 0
-      const int m = (int)((need + v - 1) / v);
-      const int k = c_gt + m;
-      int slots = k - c_above;  // filled from the near-tie group, lowest index first
-      int taken = 0;
-#pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) {
-        const bool above = fx[jj] != INT64_MIN && fx[jj] > hi;
-        const bool near = fx[jj] != INT64_MIN && fx[jj] >= lo && fx[jj] <= hi;
-        const uint32_t nb_bal = __ballot_sync(0xffffffffu, near);
-        // rank of this lane's near block among near blocks of lower index
-        const int rank = taken + __popc(nb_bal & ((1u << lane) - 1u));
-        const bool pick = above || (near && rank < slots);
-        taken += __popc(nb_bal);
-        const uint32_t bal = __ballot_sync(0xffffffffu, pick);
-        if (lane == jj) sel_word_mine = bal;
-      }
+      sel_word_mine = eq6_step_word<NJ>(fx, target, p.tol_fx, lane);
     }
     word |= sel_word_mine;
   }
@@ -429,7 +337,9 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   const int64_t rows = (int64_t)s.bh_count * s.nb;
   const unsigned grid_rows = (unsigned)((rows + 7) / 8);
   const int rounds = (s.nb + 31) / 32;
-  if (rounds <= 1) select_rows_kernel<1><<<grid_rows, 256, 0, stream>>>(p);
+  if (s.finalize_only) {
+    // the row bitmasks and counts come from the discovery epilogue
+  } else if (rounds <= 1) select_rows_kernel<1><<<grid_rows, 256, 0, stream>>>(p);
   else if (rounds <= 2) select_rows_kernel<2><<<grid_rows, 256, 0, stream>>>(p);
   else if (rounds <= 4) select_rows_kernel<4><<<grid_rows, 256, 0, stream>>>(p);
   else if (rounds <= 8) select_rows_kernel<8><<<grid_rows, 256, 0, stream>>>(p);

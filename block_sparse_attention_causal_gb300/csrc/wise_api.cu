@@ -126,9 +126,21 @@ size_t lam_bytes(const Shape& s) {
   return (size_t)(s.bh * per_bh * 128 * sizeof(float));
 }
 
+int64_t fixed_point(double x);
+
+// One step of a selection window fused into discovery (see AttnParams).
+struct FusedSelect {
+  uint32_t* bits;
+  int32_t* counts;
+  int64_t target_fx, tol_fx;
+  int32_t nwords, first, last;
+  uint32_t flags;
+};
+
 int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,
                      float* mass, void* ws, const int32_t* row_ptr, const int32_t* col_idx, int64_t col_cap,
-                     const int32_t* tile_order, bool sparse, cudaStream_t stream) {
+                     const int32_t* tile_order, bool sparse, cudaStream_t stream,
+                     const FusedSelect* fs = nullptr) {
   const Shape s = shape_of(desc);
   uint32_t* err = error_word();
   if (!err) return WISE_ERR_CUDA;
@@ -168,6 +180,16 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
   p.tile_order = tile_order;
   p.n_units = s.n_units;
   p.err = err;
+  if (fs) {
+    p.sel_bits = fs->bits;
+    p.sel_counts = fs->counts;
+    p.sel_target_fx = fs->target_fx;
+    p.sel_tol_fx = fs->tol_fx;
+    p.sel_nwords = fs->nwords;
+    p.sel_first = fs->first;
+    p.sel_last = fs->last;
+    p.sel_flags = fs->flags;
+  }
   cudaError_t e;
   switch (s.d) {
     case 64: e = launch_attn_d64(s.bn, sparse, maps, p, stream); break;
@@ -318,6 +340,82 @@ int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int
   sl.units_per_bh = s.n_qtiles;
   sl.qb_per_unit = 128 / s.bn;
   sl.group_heads = s.group_heads;
+  sl.err = err;
+  cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
+}
+
+// Largest nb of the fused selection (eight 32-block rounds per row in the
+// epilogue warps' registers).
+constexpr int kFusedSelectMaxBlocks = 256;
+
+int wise_attn_discover_select(const wise_attn_desc* desc, const void* q, const void* k, const void* v, void* o,
+                              float* lse, float* block_mass, void* workspace, size_t workspace_bytes, double eta,
+                              uint32_t flags, int32_t step, int32_t window, void* select_state,
+                              size_t select_state_bytes, wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!q || !k || !v || !o || !block_mass || !select_state) return WISE_ERR_INVALID_ARGUMENT;
+  if (window < 1 || window > 8 || step < 0 || step >= window || !(eta > 0.0 && eta < 1.0) || (flags & ~3u))
+    return WISE_ERR_INVALID_ARGUMENT;
+  const Shape s = shape_of(desc);
+  if (s.nb > kFusedSelectMaxBlocks) return WISE_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return WISE_ERR_ALIGNMENT;
+  if ((lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (reinterpret_cast<uintptr_t>(block_mass) & 3u) ||
+      (reinterpret_cast<uintptr_t>(select_state) & 15u))
+    return WISE_ERR_ALIGNMENT;
+  const size_t need = lam_bytes(s);
+  if (!workspace || workspace_bytes < need) return WISE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return WISE_ERR_ALIGNMENT;
+  if (select_state_bytes < wise_select_workspace(desc, window)) return WISE_ERR_WORKSPACE;
+  const int64_t rows = s.bh * s.nb;
+  const int64_t words = (s.nb + 31) / 32;
+  FusedSelect fs;
+  fs.bits = static_cast<uint32_t*>(select_state);
+  fs.counts = reinterpret_cast<int32_t*>(static_cast<uint32_t*>(select_state) + rows * words);
+  fs.target_fx = fixed_point(eta);
+  fs.tol_fx = fixed_point(1e-6);
+  fs.nwords = (int32_t)words;
+  fs.first = step == 0;
+  fs.last = step == window - 1;
+  fs.flags = flags;
+  return launch_attention(desc, q, k, v, o, lse, block_mass, workspace, nullptr, nullptr, 0, nullptr, false,
+                          reinterpret_cast<cudaStream_t>(stream), &fs);
+}
+
+int wise_select_finalize(const wise_attn_desc* desc, const void* select_state, size_t select_state_bytes,
+                         int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity, int32_t* tile_order, int32_t* nnz,
+                         wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!select_state || !row_ptr || !col_idx) return WISE_ERR_INVALID_ARGUMENT;
+  if (col_capacity < wise_support_capacity(desc)) return WISE_ERR_BAD_SUPPORT;
+  if (select_state_bytes < wise_select_workspace(desc, 1)) return WISE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(select_state) & 15u) || (reinterpret_cast<uintptr_t>(row_ptr) & 3u) ||
+      (reinterpret_cast<uintptr_t>(col_idx) & 3u) || (tile_order && (reinterpret_cast<uintptr_t>(tile_order) & 3u)) ||
+      (nnz && (reinterpret_cast<uintptr_t>(nnz) & 3u)))
+    return WISE_ERR_ALIGNMENT;
+  uint32_t* err = error_word();
+  if (!err) return WISE_ERR_CUDA;
+  const Shape s = shape_of(desc);
+  const int64_t rows = s.bh * s.nb;
+  const int64_t words = (s.nb + 31) / 32;
+  SelectLaunch sl;
+  memset(&sl, 0, sizeof(sl));
+  sl.window = 1;
+  sl.bh_count = (int32_t)s.bh;
+  sl.nb = s.nb;
+  sl.bits = const_cast<uint32_t*>(static_cast<const uint32_t*>(select_state));
+  sl.counts = reinterpret_cast<int32_t*>(sl.bits + rows * words);
+  sl.row_ptr = row_ptr;
+  sl.col_idx = col_idx;
+  sl.col_cap = col_capacity;
+  sl.nnz = nnz;
+  sl.tile_order = tile_order;
+  sl.units_per_bh = s.n_qtiles;
+  sl.qb_per_unit = 128 / s.bn;
+  sl.group_heads = s.group_heads;
+  sl.finalize_only = 1;
   sl.err = err;
   cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;

@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define WISE_ABI_VERSION 2
+#define WISE_ABI_VERSION 3
 
 typedef struct CUstream_st* wise_stream_t; /* same type as cudaStream_t */
 
@@ -166,6 +166,48 @@ int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int
                         double eta, uint32_t flags, int32_t* row_ptr, int32_t* col_idx,
                         int64_t col_capacity, int32_t* tile_order, int32_t* nnz,
                         void* workspace, size_t workspace_bytes, wise_stream_t stream);
+
+/*
+ * wise_attn_discover_select -- one discovery step of the selection window
+ * with that step's part of wise_select_support done in the same launch.
+ * (§5.1 Eq 6 / Appendix B Eq 18, streamed: the step supports are OR-ed into
+ * per-row bitmasks as the step's block masses are produced, so the window's
+ * mass tensors need not be kept, and no separate selection launch runs.)
+ * Computes what wise_attn_discover computes (O, LSE, the block masses into
+ * block_mass, which is required here). Then, for every query-block row, it
+ * takes the row's Eq 6 step support with exactly the arithmetic of
+ * wise_select_support, and:
+ *   - at step 0 writes it into the row's bitmask in select_state;
+ *   - at later steps ORs it in;
+ *   - at step window - 1 also adds the WISE_SUPPORT_SINK / _DIAG blocks of
+ *     `flags` and records the row's block count.
+ * After the last step, wise_select_finalize turns select_state into the CSR
+ * and work order. The steps of a window must run in order on one stream. The
+ * result is bit-identical to wise_select_support on the window's masses.
+ *   step, window : 0 <= step < window <= 8.   eta: 0 < eta < 1.
+ *   block_mass   : float32 [batch, heads, nb, nb] (device), this step's masses.
+ *   workspace    : wise_attn_discover_workspace(desc) bytes (device).
+ *   select_state : wise_select_workspace(desc, window) bytes (device, 16-byte
+ *                  aligned), kept by the caller across the window's steps;
+ *                  needs no initialisation (step 0 overwrites it).
+ * Supports nb <= 256 (WISE_ERR_UNSUPPORTED beyond: use wise_select_support).
+ */
+int wise_attn_discover_select(const wise_attn_desc* desc, const void* q, const void* k, const void* v,
+                              void* o, float* lse, float* block_mass, void* workspace,
+                              size_t workspace_bytes, double eta, uint32_t flags, int32_t step,
+                              int32_t window, void* select_state, size_t select_state_bytes,
+                              wise_stream_t stream);
+
+/*
+ * wise_select_finalize -- the CSR schedule of the support accumulated by a
+ * window of wise_attn_discover_select steps (Appendix B "Sparse-kernel
+ * implementation"): row_ptr, ascending col_idx, nnz and the late-step work
+ * order, with the same meaning, layouts and checks as in
+ * wise_select_support.
+ */
+int wise_select_finalize(const wise_attn_desc* desc, const void* select_state, size_t select_state_bytes,
+                         int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity, int32_t* tile_order,
+                         int32_t* nnz, wise_stream_t stream);
 
 /*
  * wise_select_support_noalloc -- wise_select_support for callers that cannot

@@ -94,6 +94,40 @@ def test_block_32_queries(lib):
     assert lib.wise_select_workspace(d, 3) > 0
 
 
+def test_fused_selection_argument_checks(lib):
+    d = _desc()  # 1 x 2 heads, n 256, d 64, block 64
+    ws = lib.wise_attn_discover_workspace(d)
+    st_bytes = lib.wise_select_workspace(d, 2)
+
+    def call(desc=d, q=16, mass=16, ws_=16, wsb=ws, eta=0.9, flags=3, step=0, window=2, state=16, sb=st_bytes):
+        return lib.wise_attn_discover_select(desc, q, 16, 16, 16, None, mass, ws_, wsb, eta, flags, step, window,
+                                             state, sb, None)
+    E = _lib
+    assert call(q=None) == E.WISE_ERR_INVALID_ARGUMENT
+    assert call(mass=None) == E.WISE_ERR_INVALID_ARGUMENT
+    assert call(state=None) == E.WISE_ERR_INVALID_ARGUMENT
+    assert call(step=2) == E.WISE_ERR_INVALID_ARGUMENT
+    assert call(step=-1) == E.WISE_ERR_INVALID_ARGUMENT
+    assert call(window=9, step=0) == E.WISE_ERR_INVALID_ARGUMENT
+    assert call(eta=1.0) == E.WISE_ERR_INVALID_ARGUMENT
+    assert call(flags=4) == E.WISE_ERR_INVALID_ARGUMENT
+    assert call(state=8) == E.WISE_ERR_ALIGNMENT
+    assert call(wsb=ws - 1) == E.WISE_ERR_WORKSPACE
+    assert call(sb=st_bytes - 1) == E.WISE_ERR_WORKSPACE
+    # the epilogue holds a row of up to 256 blocks
+    big = _desc(1, 1, 64 * 512, 64, 64)
+    assert call(desc=big, wsb=lib.wise_attn_discover_workspace(big),
+                sb=lib.wise_select_workspace(big, 2)) == E.WISE_ERR_UNSUPPORTED
+    cap = lib.wise_support_capacity(d)
+    fin = lambda **kw: lib.wise_select_finalize(d, kw.get("state", 16), kw.get("sb", st_bytes), kw.get("rp", 16), 16,
+                                                kw.get("cap", cap), None, None, None)
+    assert fin(state=None) == E.WISE_ERR_INVALID_ARGUMENT
+    assert fin(rp=None) == E.WISE_ERR_INVALID_ARGUMENT
+    assert fin(cap=cap - 1) == E.WISE_ERR_BAD_SUPPORT
+    assert fin(sb=16) == E.WISE_ERR_WORKSPACE
+    assert fin(state=8) == E.WISE_ERR_ALIGNMENT
+
+
 def test_null_and_misaligned_pointers_rejected(lib):
     d = _desc()
     assert lib.wise_attn_discover(d, None, 16, 16, 16, None, None, None, 0, None) == _lib.WISE_ERR_INVALID_ARGUMENT

@@ -617,3 +617,65 @@ def test_block32_trajectory_end_to_end():
                                   cfg.block, rp, ci)
         _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
         _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+
+
+# ------------------- selection fused into discovery (Eq 6 streamed over the window) ----
+
+@pytest.mark.parametrize("case", [(1, 2, 512, 64, 64, 2), (1, 3, 1024, 128, 128, 3), (2, 1, 480, 96, 32, 2),
+                                  (1, 2, 2048, 64, 128, 1), (1, 1, 8192, 64, 32, 2), (1, 2, 4096, 128, 128, 3)],
+                         ids=lambda c: "x".join(map(str, c)))
+@pytest.mark.parametrize("flags", [0, 3])
+def test_fused_selection_equals_separate_selection(case, flags):
+    b, h, n, d, blk, window = case
+    eta = 0.9
+    state = wise.new_select_state((b, h, n, d), blk, window)
+    masses = []
+    for w in range(window):
+        x, q, k, v = _bf16_inputs(b, h, n, d, seed=97 * w + n + blk, scale=1.5, planted=3)
+        o1, l1, m1 = wise.discover_select(q, k, v, blk, step=w, window=window, eta=eta, select_state=state,
+                                          flags=flags, out_dtype=torch.float32)
+        o2, l2, m2 = wise.discover(q, k, v, blk, out_dtype=torch.float32)
+        wise.check_device()
+        # the same kernel and arithmetic as plain discovery with masses
+        assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(m1, m2)
+        masses.append(m1.clone())
+    fused = wise.select_finalize(state, b, h, n, d, blk)
+    sep = wise.select_support(torch.stack(masses).contiguous(), n, d, blk, eta, flags)
+    wise.check_device()
+    rp = fused.row_ptr.cpu().numpy()
+    assert np.array_equal(rp, sep.row_ptr.cpu().numpy())
+    assert np.array_equal(fused.col_idx.cpu().numpy()[:rp[-1]], sep.col_idx.cpu().numpy()[:rp[-1]])
+    assert int(fused.nnz.item()) == int(sep.nnz.item()) == rp[-1]
+    assert torch.equal(fused.tile_order, sep.tile_order)
+    rp_ref, ci_ref = O.select(torch.stack(masses).cpu().numpy().astype(np.float64), eta, flags)
+    assert np.array_equal(rp, rp_ref) and np.array_equal(fused.col_idx.cpu().numpy()[:rp[-1]], ci_ref)
+    _check_tile_order(fused)
+
+
+def test_fused_selection_trajectory_matches_oracle():
+    cfg = wl.CONFIGS["tiny"]
+    state = wise.new_select_state((cfg.batch, cfg.heads, cfg.seq_len, cfg.head_dim), cfg.block, cfg.window)
+    oracle_masses = {}
+    for t in range(cfg.t_d):
+        x = wl.step_inputs(cfg, t)
+        q, k, v = (torch.from_numpy(x[i]).to(torch.bfloat16).cuda() for i in range(3))
+        if t in cfg.window_steps:
+            wise.discover_select(q, k, v, cfg.block, step=t - cfg.window_steps[0], window=cfg.window, eta=cfg.eta,
+                                 select_state=state)
+            oracle_masses[t] = x
+        else:
+            wise.discover(q, k, v, cfg.block, want_mass=False)
+    sup = wise.select_finalize(state, cfg.batch, cfg.heads, cfg.seq_len, cfg.head_dim, cfg.block)
+    wise.check_device()
+    rows = sup.to_lists()
+    nb = cfg.n_blocks
+    for bi in range(cfg.batch):
+        for hi in range(cfg.heads):
+            om = []
+            for t in cfg.window_steps:
+                x = oracle_masses[t]
+                _, _, r = O.causal_attention(*(x[i, bi, hi].astype(np.float64) for i in range(3)), cfg.block,
+                                             want_mass=True)
+                om.append(r)
+            base = (bi * cfg.heads + hi) * nb
+            _assert_support_matches(rows[base:base + nb], om, cfg, rows[base:base + nb])

@@ -51,7 +51,7 @@ struct SelectLaunch {
   int64_t col_cap;
   int32_t* nnz;
   int32_t* tile_order;
-  int32_t units_per_bh, qb_per_unit, group_heads;
+  int32_t units_per_bh, qb_per_unit;
   int32_t mode;                // 0: Eq 6; 1: MassMatched; 2: SizeMatched (window 1)
   int32_t finalize_only;       // bits and counts are already built (fused selection)
   const int32_t* ref_row_ptr;  // reference working set of the controls

@@ -17,8 +17,10 @@
 //      k-th mass with a bitwise search on counts instead of sums.
 //  finalize_kernel    : row_ptr (each CTA adds up the counts before its rows),
 //      nnz, ascending col_idx from the bitmasks, and the late-step work order:
-//      per L2 group of (batch, head) slices, units sorted by number of listed
-//      blocks, heaviest first.
+//      every unit of the launch sorted by number of listed blocks, heaviest
+//      first (ties by unit index), so that no heavy unit starts near the end
+//      of a sparse step. Shapes whose ranking does not fit in one CTA's
+//      shared memory are ranked per group of (batch, head) slices.
 #include <stdint.h>
 
 #include "internal.h"
@@ -166,8 +168,9 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
 
 constexpr int kChunkRows = 256;  // rows per finalize CTA (one per thread)
 
-// Rank the units of one L2 group by cost (listed blocks), heaviest first, ties
-// by unit index, and write their global order: a stable counting sort.
+// Rank the units of one group of (batch, head) slices by cost (listed
+// blocks), heaviest first, ties by unit index, and write their global order:
+// a stable counting sort.
 // Shared memory: cost[units] | start[maxc + 1], maxc = nb * qb_per_unit.
 __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
   const int h0 = g * p.group_heads;
@@ -228,7 +231,7 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
 // Finalize, one launch: CTAs [0, n_chunks) each take kChunkRows rows, add up
 // the counts of every earlier row themselves (no separate scan pass), write
 // their row_ptr entries and emit their rows' column lists in ascending order;
-// the remaining CTAs build the late-step work order, one L2 group each.
+// the remaining CTAs build the late-step work order, one group each.
 __global__ void __launch_bounds__(kChunkRows) finalize_kernel(const SelectParams p, int n_chunks) {
   extern __shared__ int32_t sh[];
   __shared__ int64_t red[kChunkRows / 32];
@@ -328,7 +331,16 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   p.tile_order = s.tile_order;
   p.units_per_bh = s.units_per_bh;
   p.qb_per_unit = s.qb_per_unit;
-  p.group_heads = s.group_heads;
+  // ranking groups: all slices in one group when its counting sort fits in
+  // shared memory (cost per unit + one counter per cost value)
+  {
+    constexpr size_t kOrderSmem = 200u * 1024u;
+    const size_t fixed = ((size_t)s.nb * s.qb_per_unit + 1) * sizeof(int32_t);
+    const size_t per_slice = (size_t)s.units_per_bh * sizeof(int32_t);
+    int64_t g = s.bh_count;
+    if (fixed + per_slice * (size_t)g > kOrderSmem) g = (int64_t)((kOrderSmem - fixed) / per_slice);
+    p.group_heads = (int32_t)(g < 1 ? 1 : g);
+  }
   p.mode = s.mode;
   p.ref_row_ptr = s.ref_row_ptr;
   p.ref_col_idx = s.ref_col_idx;
@@ -346,9 +358,9 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   else if (rounds <= 16) select_rows_kernel<16><<<grid_rows, 256, 0, stream>>>(p);
   else select_rows_kernel<32><<<grid_rows, 256, 0, stream>>>(p);
   const int n_chunks = (int)((rows + kChunkRows - 1) / kChunkRows);
-  const int groups = s.tile_order ? (s.bh_count + s.group_heads - 1) / s.group_heads : 0;
+  const int groups = s.tile_order ? (s.bh_count + p.group_heads - 1) / p.group_heads : 0;
   const size_t shm =
-      s.tile_order ? ((size_t)s.group_heads * s.units_per_bh + (size_t)s.nb * s.qb_per_unit + 1) * sizeof(int32_t) : 0;
+      s.tile_order ? ((size_t)p.group_heads * s.units_per_bh + (size_t)s.nb * s.qb_per_unit + 1) * sizeof(int32_t) : 0;
   if (shm > 40 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
     if (e != cudaSuccess) return e;

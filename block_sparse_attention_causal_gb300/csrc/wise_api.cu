@@ -339,7 +339,6 @@ int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int
   sl.tile_order = tile_order;
   sl.units_per_bh = s.n_qtiles;
   sl.qb_per_unit = 128 / s.bn;
-  sl.group_heads = s.group_heads;
   sl.err = err;
   cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
@@ -414,7 +413,6 @@ int wise_select_finalize(const wise_attn_desc* desc, const void* select_state, s
   sl.tile_order = tile_order;
   sl.units_per_bh = s.n_qtiles;
   sl.qb_per_unit = 128 / s.bn;
-  sl.group_heads = s.group_heads;
   sl.finalize_only = 1;
   sl.err = err;
   cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
@@ -459,7 +457,6 @@ int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_m
   sl.tile_order = tile_order;
   sl.units_per_bh = s.n_qtiles;
   sl.qb_per_unit = 128 / s.bn;
-  sl.group_heads = s.group_heads;
   sl.err = err;
   cudaError_t e = launch_select(sl, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
@@ -567,7 +564,6 @@ int wise_select_control(const wise_attn_desc* desc, const float* block_mass, int
   sl.tile_order = tile_order;
   sl.units_per_bh = s.n_qtiles;
   sl.qb_per_unit = 128 / s.bn;
-  sl.group_heads = s.group_heads;
   sl.mode = mode;
   sl.ref_row_ptr = ref_row_ptr;
   sl.ref_col_idx = ref_col_idx;

@@ -157,8 +157,8 @@ size_t wise_select_workspace(const wise_attn_desc* desc, int32_t window);
  *                row. col_capacity must be >= wise_support_capacity(desc).
  *   tile_order : int32 [wise_schedule_units(desc)] (device) or NULL: the
  *                late-step work order (execution metadata for
- *                wise_attn_sparse: heads in L2-sized groups, heavier units
- *                first within a group).
+ *                wise_attn_sparse: units with more listed blocks first,
+ *                ties by unit index).
  *   nnz        : int32 [1] (device) or NULL: total number of entries.
  *   workspace  : wise_select_workspace(desc, window) bytes (device).
  */

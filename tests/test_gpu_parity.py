@@ -147,6 +147,20 @@ def _check_tile_order(sup):
     units = int(lib.wise_schedule_units(desc))
     order = sup.tile_order.cpu().numpy()[:units]
     assert sorted(order.tolist()) == list(range(units))
+    # a work unit is one 128-row query tile of one (batch, head); its cost is
+    # the number of blocks its query blocks list. When the ranking fits in one
+    # CTA's shared memory (200 KB) every unit is ranked together: heaviest
+    # first, ties by unit index.
+    qpu = 128 // sup.block
+    nb = sup.seq_len // sup.block
+    if (units + nb * qpu + 1) * 4 <= 200 * 1024:
+        counts = np.diff(sup.row_ptr.cpu().numpy().astype(np.int64)).reshape(sup.batch * sup.heads, nb)
+        tiles = units // (sup.batch * sup.heads)
+        pad = np.zeros((sup.batch * sup.heads, tiles * qpu), np.int64)
+        pad[:, :nb] = counts
+        cost = pad.reshape(sup.batch * sup.heads, tiles, qpu).sum(-1).reshape(-1)
+        expect = np.argsort(-cost, kind="stable")
+        assert np.array_equal(order, expect)
 
 
 def test_select_on_gpu_masses_matches_oracle_select():

@@ -465,14 +465,18 @@ __device__ __forceinline__ void gather_scheduler(const AttnParams& p, const CUte
     bool alive;
   };
   GCur sc0, sc1;
+  // a CTA's first two work-order positions are fixed (2b and 2b + 1); the
+  // counter hands out the positions after the first 2 x gridDim
+  uint32_t nclaim = 0;
   auto claim = [&](GCur& sc) -> bool {
     for (;;) {
       int stop = 0;
       unsigned int x = 0u;
       if (lane == 0) {
         stop = *abort_flag;
-        if (!stop) x = atomicAdd(&sched->next, 1u);
+        if (!stop) x = (nclaim < 2u) ? 2u * blockIdx.x + nclaim : 2u * gridDim.x + atomicAdd(&sched->next, 1u);
       }
+      ++nclaim;
       if (__shfl_sync(FULLM, stop, 0)) return false;
       x = __shfl_sync(FULLM, x, 0);
       if ((int64_t)x >= p.n_units) return false;
@@ -742,11 +746,17 @@ __global__ void __launch_bounds__(512, 1)
         bool alive;
       };
       StreamCur sc0, sc1;
+      // Late steps: a CTA's first two work-order positions are fixed (2b and
+      // 2b + 1), which saves the launch-wide atomic at the start; the counter
+      // hands out the positions after the first 2 x gridDim.
+      uint32_t nclaim = SPARSE ? 0u : 2u;
       // claim the next unit with at least one entry for stream s
       auto claim = [&](StreamCur& sc) -> bool {
         for (;;) {
           if (*abort_flag) return false;
-          const unsigned int x = atomicAdd(&sched->next, 1u);
+          const unsigned int x = (nclaim < 2u) ? 2u * blockIdx.x + nclaim
+                                               : (SPARSE ? 2u * gridDim.x : 0u) + atomicAdd(&sched->next, 1u);
+          ++nclaim;
           if ((int64_t)x >= p.n_units) return false;
           const int64_t v = (SPARSE && p.tile_order != nullptr) ? (int64_t)__ldg(p.tile_order + x) : default_unit(x, p);
           if (v < 0 || v >= p.n_units) {

@@ -249,11 +249,25 @@ def run_gpu(args, rank, world):
         else:
             fn()
 
+    # host-to-device copies of a trajectory's step inputs run on rotating copy
+    # streams, so that the copy of a later step overlaps the kernels of the
+    # current one; each step's kernels wait for their own inputs only
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(4)]
+
     def trajectory(inputs, record=False, out_host=None, host_inputs=None):
         launches = 0
+        ready = {}
+        if host_inputs is not None:
+            for t in range(T):
+                cs = copy_streams[t % len(copy_streams)]
+                cs.wait_stream(stream)  # the previous use of the buffer is done
+                with torch.cuda.stream(cs):
+                    inputs[t].copy_(host_inputs[t], non_blocking=True)
+                ready[t] = torch.cuda.Event()
+                ready[t].record(cs)
         for t in range(T):
             if host_inputs is not None:
-                inputs[t].copy_(host_inputs[t], non_blocking=True)
+                stream.wait_event(ready[t])
             q, k, v = inputs[t][0], inputs[t][1], inputs[t][2]
             if t < td:
                 w = t - (td - W)

@@ -46,12 +46,21 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _check_device(name: str, t: torch.Tensor) -> None:
+    """The library launches on the current CUDA device's stream and error word,
+    so every tensor must live on that device."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{torch.cuda.current_device()} "
+                         "(select it with torch.cuda.set_device)")
+
+
 def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
     """Validates the operands; returns the number of key/value heads (fewer
     than the query heads for grouped-query attention)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        _check_device(name, t)
         if t.dtype != torch.bfloat16:
             raise ValueError(f"{name} must be bfloat16")
         if not t.is_contiguous() or t.dim() != 4:

@@ -190,6 +190,7 @@ def select_support(masses: torch.Tensor, seq_len: int, head_dim: int, block: int
     """Working-set selection from the window's masses [W, B, H, nb, nb] (f32)."""
     if not masses.is_cuda or masses.dtype != torch.float32 or masses.dim() != 5 or not masses.is_contiguous():
         raise ValueError("masses must be a contiguous float32 CUDA tensor [W, B, H, nb, nb]")
+    _check_device("masses", masses)
     lib = _lib.load()
     w, b, h, nb, nb2 = masses.shape
     if nb != nb2 or nb * block != seq_len:
@@ -290,6 +291,7 @@ def select_control(masses: torch.Tensor, reference: Support, mode: str, flags: i
         raise ValueError('mode must be "mass" or "size"')
     if not masses.is_cuda or masses.dtype != torch.float32 or masses.dim() != 4 or not masses.is_contiguous():
         raise ValueError("masses must be a contiguous float32 CUDA tensor [B, H, nb, nb]")
+    _check_device("masses", masses)
     b, h, nb, _ = masses.shape
     if (b, h, nb) != (reference.batch, reference.heads, reference.n_blocks):
         raise ValueError("masses do not match the reference support's shape")
@@ -319,6 +321,7 @@ def retained_mass(masses: torch.Tensor, support: Support, *, stream: Optional[to
     Returns (per-row fractions [B*H*nb] f32, per-batch mean [B] f64)."""
     if not masses.is_cuda or masses.dtype != torch.float32 or masses.dim() != 4 or not masses.is_contiguous():
         raise ValueError("masses must be a contiguous float32 CUDA tensor [B, H, nb, nb]")
+    _check_device("masses", masses)
     b, h, nb, _ = masses.shape
     if (b, h, nb) != (support.batch, support.heads, support.n_blocks):
         raise ValueError("masses do not match the support's shape")

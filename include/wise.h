@@ -42,8 +42,11 @@
  *   128-row query tiles, i.e. four query blocks of 32 share one tile);
  *   seq_len a positive multiple of block with seq_len / block <= 1024;
  *   batch * heads >= 1. Base pointers of Q/K/V/O must be 16-byte aligned.
- * - The library never allocates or frees memory and keeps no state besides
- *   one device error word per GPU. Calls are asynchronous and ordered on the
+ * - The library never allocates or frees memory. Its only state lives in
+ *   fixed device arrays of the library image: one error word per GPU, a ring
+ *   of 256 work counters that attention launches take in turn (each launch
+ *   leaves its counter at zero when it ends), and the scratch array of
+ *   wise_select_support_noalloc. Calls are asynchronous and ordered on the
  *   given stream (a cudaStream_t; NULL means the legacy default stream).
  * - Argument, shape and alignment errors are reported before any launch and
  *   nothing is written. A failed launch returns WISE_ERR_CUDA. Kernel-side

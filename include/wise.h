@@ -216,10 +216,11 @@ int wise_select_finalize(const wise_attn_desc* desc, const void* select_state, s
  * wise_select_support_noalloc -- wise_select_support for callers that cannot
  * allocate device memory. (Not an operation of the paper: the same selection
  * as wise_select_support, only the scratch memory comes from elsewhere.)
- * Some callers cannot call cudaMalloc or hand out a workspace: code running
- * while a CUDA graph is being captured (allocation is not allowed there),
- * engines whose memory plan is fixed before they run, or runtimes that own
- * every byte of device memory through their own pool. This variant takes the
+ * Some callers cannot call cudaMalloc or hand out a workspace: engines whose
+ * memory plan is fixed before they run, runtimes that own every byte of
+ * device memory through their own pool, and code that must not call the
+ * allocator on its path because cudaMalloc / cudaFree can synchronise the
+ * device. This variant takes the
  * same arguments minus the workspace and uses a 2 MiB scratch array that is
  * part of the library image instead, so it allocates nothing.
  *   - The scratch is held by every GPU that loads the library until the

@@ -1,6 +1,7 @@
 """The allocation-free selection entry point (wise_select_support_noalloc),
-for callers that cannot allocate device memory (e.g. while a CUDA graph is
-being captured, or under a fixed memory plan): through the C ABI its output
+for callers that cannot allocate device memory (a fixed memory plan, a runtime
+that owns all device memory, a path that must not call the allocator): through
+the C ABI its output
 must equal wise_select_support's, on two calls in a row (the shared scratch
 array keeps the previous call's contents, which must not leak into the next).
 This file is collected last so that a failure here cannot hide other tests."""

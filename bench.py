@@ -155,6 +155,15 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def setup_cost_ms(select_ms: float, mass_step_ms, dense_ms: float, window: int) -> float:
+    """Cost of building the support: the selection launch plus what each of
+    the window's discovery launches costs beyond the plain dense kernel (the
+    mass epilogue, or the fused selection); a mass step measured faster than
+    the dense kernel adds nothing."""
+    extra = 0.0 if mass_step_ms is None else max(0.0, mass_step_ms - dense_ms)
+    return select_ms + window * extra
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in ("attn_kernel.cuh", "ptx.cuh", "select_step.cuh", "internal.h"):
@@ -392,9 +401,8 @@ def run_gpu(args, rank, world):
         sel_bytes = read + (B * H * nb + 1) * 4 + rp[-1] * 4
         kern_stats["select"]["gbs"] = sel_bytes / (kern_stats["select"]["avg_ms"] * 1e-3) / 1e9
     mass_kind = "discover_select" if fused else "discover_mass"
-    setup_ms = kern_stats["select"]["avg_ms"]
-    if mass_kind in kern_stats:
-        setup_ms += W * max(0.0, kern_stats[mass_kind]["avg_ms"] - dense_ms)
+    setup_ms = setup_cost_ms(kern_stats["select"]["avg_ms"],
+                             kern_stats[mass_kind]["avg_ms"] if mass_kind in kern_stats else None, dense_ms, W)
     dominant = max((k_ for k_ in kern_stats if k_ != "select"), key=lambda k_: kern_stats[k_]["total_ms_per_step"])
     dom = kern_stats[dominant]
     achieved = dom["tflops"]

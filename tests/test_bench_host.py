@@ -26,6 +26,16 @@ def test_support_flops_counts_admissible_pairs():
     assert bench.support_flops(rp, ci, 3, blk, d) == 4.0 * d * brute
 
 
+def test_setup_cost_counts_selection_and_window_overhead():
+    # selection 0.03 ms; three window steps at 0.13 ms against a 0.12 ms
+    # dense kernel: 0.03 + 3 * 0.01
+    assert bench.setup_cost_ms(0.03, 0.13, 0.12, 3) == pytest.approx(0.06)
+    # no mass steps timed: the selection alone
+    assert bench.setup_cost_ms(0.03, None, 0.12, 3) == pytest.approx(0.03)
+    # a mass step measured below the dense kernel adds nothing
+    assert bench.setup_cost_ms(0.03, 0.11, 0.12, 3) == pytest.approx(0.03)
+
+
 def test_tile_entries_count_what_the_scheduler_forms():
     # one head, nb = 6 blocks of 32: two 128-row tiles, the second ragged
     # (query blocks 4 and 5 only). Tile 0's rows list {0, 1, 2, 3}: one

@@ -56,6 +56,64 @@ def _check_device(name: str, t: torch.Tensor) -> None:
                          "(select it with torch.cuda.set_device)")
 
 
+def _check_buffer(name: str, t: torch.Tensor, dtype: torch.dtype, shape: Sequence[int],
+                  device: torch.device) -> None:
+    """A caller-supplied output or scratch tensor. The C ABI receives bare
+    pointers and cannot see sizes, so a wrong dtype, shape or layout here
+    would let a kernel write past the allocation: rejected before any launch."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(int(x) for x in shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_bytes(name: str, t: torch.Tensor, nbytes: int, device: torch.device) -> None:
+    """A caller-supplied workspace or selection state: uint8, contiguous, on
+    `device`, and at least `nbytes` long."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != torch.uint8 or t.dim() != 1 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 1-D uint8 tensor")
+    if t.numel() < nbytes:
+        raise ValueError(f"{name} holds {t.numel()} bytes, the call needs {nbytes}")
+
+
+def _check_int32(name: str, t: torch.Tensor, min_numel: int, device: torch.device, exact: bool = False) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != torch.int32 or t.dim() != 1 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 1-D int32 tensor")
+    if (t.numel() != min_numel) if exact else (t.numel() < min_numel):
+        want = f"exactly {min_numel}" if exact else f"at least {min_numel}"
+        raise ValueError(f"{name} has {t.numel()} entries, {want} needed")
+
+
+def _check_support(name: str, sup: "Support", device: torch.device, units: int, capacity: int = 1,
+                   need_order: bool = False) -> None:
+    """The CSR tensors of a Support: int32, contiguous, on `device`, with
+    row_ptr of exactly batch*heads*nb + 1 entries, col_idx of at least
+    `capacity`, and (when present or required) a work order of at least
+    `units` entries."""
+    rows = sup.batch * sup.heads * sup.n_blocks
+    _check_int32(f"{name}.row_ptr", sup.row_ptr, rows + 1, device, exact=True)
+    _check_int32(f"{name}.col_idx", sup.col_idx, max(capacity, 1), device)
+    _check_int32(f"{name}.nnz", sup.nnz, 1, device)
+    if sup.tile_order is not None:
+        _check_int32(f"{name}.tile_order", sup.tile_order, units, device)
+    elif need_order:
+        raise ValueError(f"{name}.tile_order is required here")
+
+
 def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
     """Validates the operands; returns the number of key/value heads (fewer
     than the query heads for grouped-query attention)."""
@@ -95,18 +153,24 @@ def discover(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: int, *, w
     lib = _lib.load()
     b, h, n, d = q.shape
     desc = _desc(q.shape, block, scale, out_dtype, hk)
+    dev = q.device
     if out is None:
-        out = torch.empty((b, h, n, d), dtype=out_dtype, device=q.device)
+        out = torch.empty((b, h, n, d), dtype=out_dtype, device=dev)
+    _check_buffer("out", out, out_dtype, (b, h, n, d), dev)
     if want_lse and lse is None:
-        lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+        lse = torch.empty((b, h, n), dtype=torch.float32, device=dev)
+    if want_lse:
+        _check_buffer("lse", lse, torch.float32, (b, h, n), dev)
     nb = n // block if block > 0 else 0
     ws_bytes = 0
     if want_mass:
         if mass is None:
-            mass = torch.empty((b, h, nb, nb), dtype=torch.float32, device=q.device)
+            mass = torch.empty((b, h, nb, nb), dtype=torch.float32, device=dev)
+        _check_buffer("mass", mass, torch.float32, (b, h, nb, nb), dev)
         ws_bytes = int(lib.wise_attn_discover_workspace(desc))
         if workspace is None:
-            workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+            workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        _check_bytes("workspace", workspace, ws_bytes, dev)
     else:
         mass = None
     st = lib.wise_attn_discover(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), _ptr(lse),
@@ -142,16 +206,23 @@ def discover_select(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: in
     lib = _lib.load()
     b, h, n, d = q.shape
     desc = _desc(q.shape, block, scale, out_dtype, hk)
+    dev = q.device
     if out is None:
-        out = torch.empty((b, h, n, d), dtype=out_dtype, device=q.device)
+        out = torch.empty((b, h, n, d), dtype=out_dtype, device=dev)
+    _check_buffer("out", out, out_dtype, (b, h, n, d), dev)
     if want_lse and lse is None:
-        lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+        lse = torch.empty((b, h, n), dtype=torch.float32, device=dev)
+    if want_lse:
+        _check_buffer("lse", lse, torch.float32, (b, h, n), dev)
     nb = n // block
     if mass is None:
-        mass = torch.empty((b, h, nb, nb), dtype=torch.float32, device=q.device)
+        mass = torch.empty((b, h, nb, nb), dtype=torch.float32, device=dev)
+    _check_buffer("mass", mass, torch.float32, (b, h, nb, nb), dev)
     ws_bytes = int(lib.wise_attn_discover_workspace(desc))
     if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    _check_bytes("workspace", workspace, ws_bytes, dev)
+    _check_bytes("select_state", select_state, int(lib.wise_select_workspace(desc, window)), dev)
     st = lib.wise_attn_discover_select(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), _ptr(lse),
                                        mass.data_ptr(), workspace.data_ptr(), workspace.numel(), float(eta), flags,
                                        step, window, select_state.data_ptr(), select_state.numel(),
@@ -204,9 +275,13 @@ def select_support(masses: torch.Tensor, seq_len: int, head_dim: int, block: int
                           torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
                           torch.empty(max(units, 1), dtype=torch.int32, device=dev),
                           torch.empty(1, dtype=torch.int32, device=dev), b, h, seq_len, head_dim, block)
+    if (support.batch, support.heads, support.seq_len, support.block) != (b, h, seq_len, block):
+        raise ValueError("support was built for a different shape")
+    _check_support("support", support, dev, units, cap, need_order=True)
     ws_bytes = int(lib.wise_select_workspace(desc, w))
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    _check_bytes("workspace", workspace, ws_bytes, dev)
     st = lib.wise_select_support(desc, masses.data_ptr(), w, float(eta), flags, support.row_ptr.data_ptr(),
                                  support.col_idx.data_ptr(), support.col_idx.numel(),
                                  support.tile_order.data_ptr(), support.nnz.data_ptr(), workspace.data_ptr(),
@@ -227,10 +302,15 @@ def sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, support: Support, 
     if (b, h, n, d) != (support.batch, support.heads, support.seq_len, support.head_dim):
         raise ValueError("support was built for a different shape")
     desc = _desc(q.shape, support.block, scale, out_dtype, hk)
+    dev = q.device
+    _check_support("support", support, dev, int(lib.wise_schedule_units(desc)))
     if out is None:
-        out = torch.empty((b, h, n, d), dtype=out_dtype, device=q.device)
+        out = torch.empty((b, h, n, d), dtype=out_dtype, device=dev)
+    _check_buffer("out", out, out_dtype, (b, h, n, d), dev)
     if want_lse and lse is None:
-        lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+        lse = torch.empty((b, h, n), dtype=torch.float32, device=dev)
+    if want_lse:
+        _check_buffer("lse", lse, torch.float32, (b, h, n), dev)
     st = lib.wise_attn_sparse(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), support.row_ptr.data_ptr(),
                               support.col_idx.data_ptr(), support.col_idx.numel(),
                               support.tile_order.data_ptr() if (use_schedule and support.tile_order is not None)
@@ -250,12 +330,19 @@ def select_finalize(select_state: torch.Tensor, batch: int, heads: int, seq_len:
     nb = seq_len // block
     cap = int(lib.wise_support_capacity(desc))
     units = int(lib.wise_schedule_units(desc))
+    if cap <= 0:
+        raise ValueError("unsupported shape")
+    _check_device("select_state", select_state)
     dev = select_state.device
+    _check_bytes("select_state", select_state, int(lib.wise_select_workspace(desc, 1)), dev)
     if support is None:
         support = Support(torch.empty(batch * heads * nb + 1, dtype=torch.int32, device=dev),
                           torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
                           torch.empty(max(units, 1), dtype=torch.int32, device=dev),
                           torch.empty(1, dtype=torch.int32, device=dev), batch, heads, seq_len, head_dim, block)
+    if (support.batch, support.heads, support.seq_len, support.block) != (batch, heads, seq_len, block):
+        raise ValueError("support was built for a different shape")
+    _check_support("support", support, dev, units, cap, need_order=True)
     st = lib.wise_select_finalize(desc, select_state.data_ptr(), select_state.numel(), support.row_ptr.data_ptr(),
                                   support.col_idx.data_ptr(), support.col_idx.numel(),
                                   support.tile_order.data_ptr(), support.nnz.data_ptr(), _stream_handle(stream))
@@ -300,6 +387,7 @@ def select_control(masses: torch.Tensor, reference: Support, mode: str, flags: i
     cap = int(lib.wise_support_capacity(desc))
     units = int(lib.wise_schedule_units(desc))
     dev = masses.device
+    _check_support("reference", reference, dev, units)
     out = Support(torch.empty(b * h * nb + 1, dtype=torch.int32, device=dev),
                   torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
                   torch.empty(max(units, 1), dtype=torch.int32, device=dev),
@@ -327,6 +415,7 @@ def retained_mass(masses: torch.Tensor, support: Support, *, stream: Optional[to
         raise ValueError("masses do not match the support's shape")
     lib = _lib.load()
     desc = _lib.make_desc(support.batch, support.heads, support.seq_len, support.head_dim, support.block)
+    _check_support("support", support, masses.device, int(lib.wise_schedule_units(desc)))
     rows = torch.empty(b * h * nb, dtype=torch.float32, device=masses.device)
     mean = torch.empty(b, dtype=torch.float64, device=masses.device)
     st = lib.wise_support_retained_mass(desc, masses.data_ptr(), support.row_ptr.data_ptr(),
@@ -347,7 +436,11 @@ def support_jaccard(a: Support, b: Support, *, stream: Optional[torch.cuda.Strea
     lib = _lib.load()
     desc = _lib.make_desc(*shape)
     rows = a.batch * a.heads * a.n_blocks
+    _check_device("a.row_ptr", a.row_ptr)
     dev = a.row_ptr.device
+    units = int(lib.wise_schedule_units(desc))
+    _check_support("a", a, dev, units)
+    _check_support("b", b, dev, units)
     row_counts = torch.empty((rows, 2), dtype=torch.int32, device=dev)
     counts = torch.empty((a.batch, 2), dtype=torch.int64, device=dev)
     jac = torch.empty(a.batch, dtype=torch.float64, device=dev)

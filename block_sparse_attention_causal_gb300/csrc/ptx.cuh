@@ -70,7 +70,9 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // TAG gives each warp role of a kernel its own out-of-line copy: a function
 // called from regions with different setmaxnreg register counts cannot be
 // register-allocated.
-template <int TAG>
+// LIMIT_NS is the time limit (kWaitLimitNs everywhere except the library's
+// self-check of this path, which shortens it).
+template <int TAG, uint64_t LIMIT_NS = kWaitLimitNs>
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                             uint32_t* err_word) {
   const uint64_t t0 = global_timer_ns();
@@ -78,7 +80,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > LIMIT_NS) {
         *abort_flag = 1;
         atomicOr(err_word, kErrTimeout);
         return false;
@@ -90,11 +92,11 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 // Wait for the phase of `bar` with the given parity. Gives up (returns false)
 // when another role of the CTA has aborted or after kWaitLimitNs, in which
 // case it raises the abort flag and records kErrTimeout.
-template <int TAG = 0>
+template <int TAG = 0, uint64_t LIMIT_NS = kWaitLimitNs>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err_word) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow<TAG>(bar, parity, abort_flag, err_word);
+  return mbar_wait_slow<TAG, LIMIT_NS>(bar, parity, abort_flag, err_word);
 }
 
 // ----------------------------------------------------------------------- TMA

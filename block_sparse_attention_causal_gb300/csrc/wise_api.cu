@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -222,6 +223,21 @@ uint8_t* select_scratch() {
     g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
   }
   return g_scratch_ptr[dev];
+}
+
+// Self-check of the bounded wait: one thread waits on an mbarrier that
+// nothing arrives on, through the same wait routine as the attention kernels
+// but with a 20 ms limit. The wait expires, kErrTimeout is recorded, and the
+// kernel returns (no copy or MMA is in flight, so nothing needs draining).
+constexpr uint64_t kSelfCheckWaitNs = 20000000ull;
+__global__ void wait_expiry_kernel(uint32_t* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  mbar_wait<6, kSelfCheckWaitNs>(&bar, 0, &abort_flag, err);
 }
 
 }  // namespace
@@ -597,6 +613,27 @@ int wise_validate_support(const wise_attn_desc* desc, const int32_t* row_ptr, co
     if (((flags & WISE_SUPPORT_SINK) && !has0) || ((flags & WISE_SUPPORT_DIAG) && !hasq)) return WISE_ERR_BAD_SUPPORT;
   }
   return WISE_OK;
+}
+
+int wise_validate_schedule(const wise_attn_desc* desc, const int32_t* tile_order) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!tile_order) return WISE_ERR_INVALID_ARGUMENT;
+  const int64_t units = shape_of(desc).n_units;
+  std::vector<uint8_t> seen((size_t)units, 0);
+  for (int64_t x = 0; x < units; ++x) {
+    const int32_t u = tile_order[x];
+    if (u < 0 || u >= units || seen[(size_t)u]) return WISE_ERR_BAD_SUPPORT;
+    seen[(size_t)u] = 1;
+  }
+  return WISE_OK;
+}
+
+int wise_wait_expiry_check(wise_stream_t stream) {
+  uint32_t* err = error_word();
+  if (!err) return WISE_ERR_CUDA;
+  wait_expiry_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);
+  return cudaGetLastError() == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
 }
 
 int wise_device_status(wise_stream_t stream) {

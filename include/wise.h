@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define WISE_ABI_VERSION 3
+#define WISE_ABI_VERSION 4
 
 typedef struct CUstream_st* wise_stream_t; /* same type as cudaStream_t */
 
@@ -339,6 +339,28 @@ int wise_support_jaccard(const wise_attn_desc* desc, const int32_t* row_ptr_a, c
  * WISE_ERR_BAD_SUPPORT. */
 int wise_validate_support(const wise_attn_desc* desc, const int32_t* row_ptr_host,
                           const int32_t* col_idx_host, uint32_t flags);
+
+/* Host-side check of a late-step work order (host pointer): tile_order must
+ * hold every unit 0 .. wise_schedule_units(desc) - 1 exactly once, as
+ * wise_select_support writes it (Appendix B "Sparse-kernel implementation"
+ * fixes the CSR, not an order; the order is this library's schedule). With a
+ * duplicated unit two CTAs would compute and write the same rows; a missing
+ * unit would never be written. wise_attn_sparse only range-checks the entries
+ * it reads. Returns WISE_OK, WISE_ERR_BAD_SUPPORT, or WISE_ERR_INVALID_ARGUMENT
+ * for a NULL pointer or a bad descriptor. */
+int wise_validate_schedule(const wise_attn_desc* desc, const int32_t* tile_order_host);
+
+/* Self-check of the library's failure handling (no counterpart in the paper).
+ * Every wait in the kernels is bounded: when a wait runs out (2 s), the kernel
+ * records WISE_ERR_DEVICE_TIMEOUT in the device error word, lets its own
+ * copies finish and returns, so the CUDA context stays usable. This call
+ * launches one single-thread kernel that waits, through that same wait
+ * routine, on a barrier nothing arrives on, with the limit shortened to 20 ms.
+ * The wait runs out and the kernel returns; it touches no memory but the
+ * error word. Afterwards wise_device_status() reports
+ * WISE_ERR_DEVICE_TIMEOUT (and clears the word). Returns WISE_OK once the
+ * kernel is queued on `stream`, WISE_ERR_CUDA if the launch failed. */
+int wise_wait_expiry_check(wise_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device: WISE_OK, WISE_ERR_BAD_SUPPORT, WISE_ERR_DEVICE_TIMEOUT, or

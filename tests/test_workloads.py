@@ -41,3 +41,13 @@ def test_config_table():
     assert wl.CONFIGS["tiny"].window_steps == [0, 1]
     assert wl.CONFIGS["8k_b4"].window_steps == [0, 1, 2, 3]
     assert set(k for k in wl.CONFIGS if k.startswith("sweep")) == {"sweep_2k", "sweep_4k", "sweep_8k", "sweep_16k", "sweep_32k"}
+
+
+def test_parallel_bf16_generation_matches_the_serial_generator():
+    cfg = wl.CONFIGS["tiny"].replace(heads=3)
+    serial = wl.trajectory_inputs(cfg, [0, 3])
+    for procs in (1, 2):
+        bits = wl.trajectory_inputs_bf16(cfg, [0, 3], processes=procs)
+        for t in (0, 3):
+            assert bits[t].dtype == np.uint16
+            assert np.array_equal(bits[t], wl.bf16_bits(serial[t]))

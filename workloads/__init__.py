@@ -157,6 +157,47 @@ def trajectory_inputs(cfg: WorkloadConfig, steps: Iterable[int], seed: int = 0,
     return res
 
 
+def _head_bits(args):
+    """Worker of trajectory_inputs_bf16: one (batch, head) slice at the listed
+    steps, as bf16 bit patterns [len(steps), 3, n, d]."""
+    cfg, seed, steps, b, h = args
+    g = HeadGenerator(cfg, b, h, seed)
+    return b, h, np.stack([bf16_bits(g.step(t)) for t in steps])
+
+
+def trajectory_inputs_bf16(cfg: WorkloadConfig, steps: Iterable[int], seed: int = 0,
+                           processes: Optional[int] = None) -> Dict[int, np.ndarray]:
+    """The values of trajectory_inputs, as bf16 bit patterns (uint16 arrays
+    [3, B, H, n, d]), drawn by a pool of `processes` worker processes (default:
+    the usable cores, at most 32). Each (batch, head) slice comes from its own
+    generator, so the result does not depend on the number of processes. The
+    pool uses the 'spawn' start method, so it is safe to call after CUDA has
+    been initialised in the calling process."""
+    import multiprocessing as mp
+    import os
+    steps = list(steps)
+    shape = (3, cfg.batch, cfg.heads, cfg.seq_len, cfg.head_dim)
+    res = {t: np.empty(shape, np.uint16) for t in steps}
+    jobs = [(cfg, seed, steps, b, h) for b in range(cfg.batch) for h in range(cfg.heads)]
+    if processes is None:
+        processes = min(32, len(os.sched_getaffinity(0)))
+    processes = max(1, min(processes, len(jobs)))
+
+    def put(item):
+        b, h, bits = item
+        for i, t in enumerate(steps):
+            res[t][:, b, h] = bits[i]
+
+    if processes == 1:
+        for j in jobs:
+            put(_head_bits(j))
+    else:
+        with mp.get_context("spawn").Pool(processes) as pool:
+            for item in pool.imap_unordered(_head_bits, jobs):
+                put(item)
+    return res
+
+
 def random_support(n_blocks: int, density: float, rng: np.random.Generator,
                    sink: bool = True, diag: bool = True) -> List[List[int]]:
     """A random causal block support (list of ascending key blocks per query

@@ -356,7 +356,7 @@ static __device__ __noinline__ void select_row_fused(const AttnParams& p, int bh
     const int b = jj * 32 + lane;
     fx[jj] = (b <= q) ? mass_fx(__ldcg(src + b)) : INT64_MIN;
   }
-  uint32_t word = eq6_step_word<NJ, true>(fx, p.sel_target_fx, p.sel_tol_fx, lane);
+  uint32_t word = eq6_step_word_compact<NJ>(fx, p.sel_target_fx, p.sel_tol_fx, lane);
   uint32_t* dst = p.sel_bits + row * p.sel_nwords;
   if (!p.sel_first && lane < p.sel_nwords) word |= __ldcg(dst + lane);  // union with the window's earlier steps
   if (p.sel_last) {
@@ -765,6 +765,8 @@ __global__ void __launch_bounds__(512, 1)
           }
           const int id = (int)v;
           const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
+          // Q of the unit into L2 ahead of its TMA load, while the CSR is read
+          for (int c = 0; c < C::NCH; ++c) tma_prefetch_l2_2d(&tm_q, c * C::CH, bh * p.n + t * 128);
           if (SPARSE) sc.cur.init_sparse(t, bh, p, C::ENT_PER_TILE);
           else sc.cur.init_dense(t, p, C::KW);
           if (!sc.cur.next(sc.pblk, sc.pmask)) {
@@ -776,8 +778,6 @@ __global__ void __launch_bounds__(512, 1)
           sc.cnt = 0;
           // the key/value head of query head bh (grouped-query attention)
           sc.kvrow0 = (uint32_t)(((bh / p.heads) * (p.heads / p.kv_group) + (bh % p.heads) / p.kv_group) * p.n);
-          // Q of the unit into L2 ahead of its TMA load
-          for (int c = 0; c < C::NCH; ++c) tma_prefetch_l2_2d(&tm_q, c * C::CH, bh * p.n + t * 128);
           return true;
         }
       };
@@ -799,6 +799,30 @@ __global__ void __launch_bounds__(512, 1)
         sc.alive = claim(sc);
         return sc.alive || publish(0u, 0u, kEntMark | sflag);
       };
+      if (SPARSE) {
+        // The reads behind the CTA's first two claims, both units at once:
+        // their work-order entries, then their CSR row starts, then a
+        // prefetch of their first column entries. Each claim below then
+        // finds its data in L1 instead of waiting on three dependent loads
+        // in turn, and the launch's first records are published sooner.
+        int64_t u[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int64_t x = 2 * (int64_t)blockIdx.x + i;
+          u[i] = (x >= p.n_units) ? -1 : (p.tile_order != nullptr) ? (int64_t)__ldg(p.tile_order + x) : default_unit(x, p);
+        }
+        int32_t a[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const bool in = u[i] >= 0 && u[i] < p.n_units;
+          const int64_t r = in ? (u[i] / p.n_qtiles) * p.nb + (u[i] % p.n_qtiles) * C::ENT_PER_TILE : 0;
+          a[i] = in ? __ldg(p.row_ptr + r) : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (a[i] >= 0 && (int64_t)a[i] < p.col_cap)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(p.col_idx + a[i]));
+      }
       sc0.alive = claim(sc0);
       if (!sc0.alive) ok = publish(0u, 0u, kEntMark);
       sc1.alive = ok && claim(sc1);

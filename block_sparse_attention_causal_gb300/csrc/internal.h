@@ -69,6 +69,17 @@ cudaError_t launch_attn_d128(int block, bool sparse, const CUtensorMap* maps, co
 
 cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream);
 
+// Selection workspace layout: the row bitmasks [rows][nwords] and counts
+// [rows] (int32), then, 16-byte aligned, the look-back state of the row_ptr
+// scan (one 64-bit word per chunk of kSelectChunkRows rows plus a ticket).
+constexpr int kSelectChunkRows = 256;
+__host__ __device__ inline int64_t select_lookback_offset(int64_t rows, int64_t nwords) {
+  return ((rows * nwords + rows) * 4 + 15) / 16 * 16;
+}
+__host__ __device__ inline int64_t select_lookback_bytes(int64_t rows) {
+  return ((rows + kSelectChunkRows - 1) / kSelectChunkRows) * 8 + 16;
+}
+
 // Support diagnostics (diag_kernel.cu): retained future attention mass and
 // the Jaccard index of two supports.
 struct DiagLaunch {

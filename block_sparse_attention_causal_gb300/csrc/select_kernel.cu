@@ -15,7 +15,8 @@
 //      row's mass covered by the reference, summed in the same fixed point;
 //      SizeMatched (Eq 22) keeps the reference's block count k and finds the
 //      k-th mass with a bitwise search on counts instead of sums.
-//  finalize_kernel    : row_ptr (each CTA adds up the counts before its rows),
+//  finalize_kernel    : row_ptr (each chunk of rows takes the count of the
+//      rows before it from the chunks before it, by a decoupled look-back),
 //      nnz, ascending col_idx from the bitmasks, and the late-step work order:
 //      every unit of the launch sorted by number of listed blocks, heaviest
 //      first (ties by unit index), so that no heavy unit starts near the end
@@ -52,25 +53,86 @@ struct SelectParams {
   const int32_t* ref_row_ptr;  // reference working set (modes 1 and 2)
   const int32_t* ref_col_idx;
   int64_t ref_cap;
+  uint64_t* lb;      // look-back state of the row_ptr scan (zeroed before finalize)
+  int32_t lb_words;  // its size in 64-bit words
   uint32_t* err;
 };
 
-// 8 warps per CTA, one row per warp; NJ rounds of 32 blocks cover nb <= 32 NJ.
+// Word `lane` of the union over the window of one row's Eq 6 step supports,
+// with NJ rounds of 32 blocks covering the row's q + 1 admissible blocks.
+// The next step's masses are loaded while the current step is selected.
 template <int NJ>
-__global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) {
+__device__ __forceinline__ uint32_t union_eq6(const SelectParams& p, int bh, int q, int lane) {
+  const int nadm = q + 1;
+  auto src = [&](int w) { return p.mass + (((int64_t)w * p.bh_count + bh) * p.nb + q) * p.nb; };
+  float cur[NJ], nxt[NJ];
+#pragma unroll
+  for (int jj = 0; jj < NJ; ++jj) {
+    const int b = jj * 32 + lane;  // coalesced load order: jj-major
+    cur[jj] = (b < nadm) ? __ldg(src(0) + b) : 0.f;
+  }
+  uint32_t word = 0;
+  for (int w = 0; w < p.window; ++w) {
+    if (w + 1 < p.window) {
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) {
+        const int b = jj * 32 + lane;
+        nxt[jj] = (b < nadm) ? __ldg(src(w + 1) + b) : 0.f;
+      }
+    }
+    int64_t fx[NJ];
+    uint32_t key[NJ];
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) {
+      const bool adm = jj * 32 + lane < nadm;
+      fx[jj] = adm ? mass_fx(cur[jj]) : INT64_MIN;
+      key[jj] = adm ? mass_key(cur[jj]) : 0u;
+    }
+    word |= eq6_step_word<NJ>(fx, key, p.target_fx, p.tol_fx, lane);
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) cur[jj] = nxt[jj];
+  }
+  return word;
+}
+
+// The Eq 6 union of one row with the fewest rounds that cover its q + 1
+// admissible blocks (a row near the start of the sequence costs less than
+// one near its end).
+template <int NJ>
+__device__ __forceinline__ uint32_t union_eq6_any(const SelectParams& p, int bh, int q, int lane) {
+  const int nadm = q + 1;
+  if (NJ == 1 || nadm <= 32) return union_eq6<1>(p, bh, q, lane);
+  if (NJ == 2 || nadm <= 64) return union_eq6<(NJ < 2 ? NJ : 2)>(p, bh, q, lane);
+  if (NJ == 4 || nadm <= 128) return union_eq6<(NJ < 4 ? NJ : 4)>(p, bh, q, lane);
+  if (NJ == 8 || nadm <= 256) return union_eq6<(NJ < 8 ? NJ : 8)>(p, bh, q, lane);
+  if (NJ == 16 || nadm <= 512) return union_eq6<(NJ < 16 ? NJ : 16)>(p, bh, q, lane);
+  return union_eq6<NJ>(p, bh, q, lane);
+}
+
+// 8 warps per CTA, one row per warp; NJ rounds of 32 blocks cover nb <= 32 NJ.
+// Up to 8 rounds the registers are capped so that four CTAs share an SM.
+template <int NJ>
+__global__ void __launch_bounds__(256, (NJ <= 8) ? 4 : 1) select_rows_kernel(const SelectParams p) {
   __shared__ uint32_t refbits[8][32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  // the finalize kernel that follows starts from a cleared look-back state
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.lb_words; i += blockDim.x) p.lb[i] = 0ull;
   const int64_t row = (int64_t)blockIdx.x * 8 + wid;
   const int64_t rows = (int64_t)p.bh_count * p.nb;
   if (row >= rows) return;
   const int bh = (int)(row / p.nb);
   const int q = (int)(row % p.nb);
   const int nadm = q + 1;  // admissible key blocks 0..q
-  // Controls: the reference row as a bitmask (entries outside 0..q flagged and
-  // skipped; repeated entries count once); in_ref[jj] is this lane's block.
-  bool in_ref[NJ];
-  int ref_k = 0;
-  if (p.mode != 0) {
+  uint32_t word = 0;  // word `lane` of the row's union bitmask
+  if (p.mode == 0) {
+    word = union_eq6_any<NJ>(p, bh, q, lane);
+  } else {
+    // Controls: the reference row as a bitmask (entries outside 0..q flagged
+    // and skipped; repeated entries count once); in_ref[jj] is this lane's
+    // block.
+    bool in_ref[NJ];
+    int ref_k = 0;
     refbits[wid][lane] = 0u;
     __syncwarp();
     int32_t a = __ldg(p.ref_row_ptr + row), b = __ldg(p.ref_row_ptr + row + 1);
@@ -89,74 +151,76 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) in_ref[jj] = (refbits[wid][jj] >> lane) & 1u;
     ref_k = warp_sum32(__popc(refbits[wid][lane]));
-  }
-  uint32_t word = 0;  // word `lane` of the row's union bitmask
-  for (int w = 0; w < p.window; ++w) {
-    const float* src = p.mass + (((int64_t)w * p.bh_count + bh) * p.nb + q) * p.nb;
-    int64_t fx[NJ];
-#pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) {
-      const int b = jj * 32 + lane;  // coalesced load order: jj-major
-      fx[jj] = (b < nadm) ? mass_fx(__ldg(src + b)) : INT64_MIN;
-    }
-    uint32_t sel_word_mine = 0;  // the word this lane will hold (word index = lane)
-    int64_t target = p.target_fx;
-    if (p.mode == 1) {  // MassMatched: the mass the reference covers at this step
-      int64_t t = 0;
-#pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) t += (in_ref[jj] && fx[jj] > 0) ? fx[jj] : 0;
-      target = warp_sum_u63(t);
-    }
-    if ((p.mode == 1 && target <= 0) || (p.mode == 2 && ref_k == 0)) {
-      // an empty reference (or one without mass) selects nothing
-    } else if (p.mode == 2) {
-      // SizeMatched: the ref_k largest masses; v = the largest value with at
-      // least ref_k admissible blocks >= v
-      int64_t v = 0;
-      if (ref_k < nadm) {
-        if (NJ == 1) {
-          // one value per lane: v = the largest value with >= ref_k values >= it
-          int c = 0;
-#pragma unroll 8
-          for (int j = 0; j < 32; ++j) c += (__shfl_sync(0xffffffffu, fx[0], j) >= fx[0]) ? 1 : 0;
-          v = warp_max64((fx[0] != INT64_MIN && c >= ref_k) ? fx[0] : 0);
-        } else {
-          int64_t max_pos = 0;
-#pragma unroll
-          for (int jj = 0; jj < NJ; ++jj) max_pos = max(max_pos, fx[jj]);
-          max_pos = warp_max64(max_pos);
-          for (int bit = 63 - __clzll(max_pos > 0 ? max_pos : 1); bit >= 0; --bit) {
-            const int64_t cand = v | (int64_t(1) << bit);
-            int cnt = 0;
-#pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) cnt += (fx[jj] >= cand) ? 1 : 0;
-            if (warp_sum32(cnt) >= ref_k) v = cand;
-          }
-        }
-      }
-      int c_above = 0;
-      const int64_t hi = v + p.tol_fx, lo = v - p.tol_fx;
-#pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) c_above += (fx[jj] != INT64_MIN && fx[jj] > hi) ? 1 : 0;
-      c_above = warp_sum32(c_above);
-      const int k = min(ref_k, nadm);
-      int slots = k - c_above;  // filled from the near-tie group, lowest index first
-      int taken = 0;
+    for (int w = 0; w < p.window; ++w) {
+      const float* src = p.mass + (((int64_t)w * p.bh_count + bh) * p.nb + q) * p.nb;
+      int64_t fx[NJ];
+      uint32_t key[NJ];
 #pragma unroll
       for (int jj = 0; jj < NJ; ++jj) {
-        const bool above = fx[jj] != INT64_MIN && fx[jj] > hi;
-        const bool near = fx[jj] != INT64_MIN && fx[jj] >= lo && fx[jj] <= hi;
-        const uint32_t nb_bal = __ballot_sync(0xffffffffu, near);
-        const int rank = taken + __popc(nb_bal & ((1u << lane) - 1u));
-        const bool pick = above || (near && rank < slots);
-        taken += __popc(nb_bal);
-        const uint32_t bal = __ballot_sync(0xffffffffu, pick);
-        if (lane == jj) sel_word_mine = bal;
+        const int bb = jj * 32 + lane;  // coalesced load order: jj-major
+        const float m = (bb < nadm) ? __ldg(src + bb) : 0.f;
+        fx[jj] = (bb < nadm) ? mass_fx(m) : INT64_MIN;
+        key[jj] = (bb < nadm) ? mass_key(m) : 0u;
       }
-    } else {
-      sel_word_mine = eq6_step_word<NJ>(fx, target, p.tol_fx, lane);
+      uint32_t sel_word_mine = 0;  // the word this lane will hold (word index = lane)
+      int64_t target = 0;
+      if (p.mode == 1) {  // MassMatched: the mass the reference covers at this step
+        int64_t t = 0;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) t += (in_ref[jj] && fx[jj] > 0) ? fx[jj] : 0;
+        target = warp_sum_u63(t);
+      }
+      if ((p.mode == 1 && target <= 0) || (p.mode == 2 && ref_k == 0)) {
+        // an empty reference (or one without mass) selects nothing
+      } else if (p.mode == 2) {
+        // SizeMatched: the ref_k largest masses; v = the largest value with at
+        // least ref_k admissible blocks >= v
+        int64_t v = 0;
+        if (ref_k < nadm) {
+          if (NJ == 1) {
+            // one value per lane: v = the largest value with >= ref_k values >= it
+            int c = 0;
+#pragma unroll 8
+            for (int j = 0; j < 32; ++j) c += (__shfl_sync(0xffffffffu, fx[0], j) >= fx[0]) ? 1 : 0;
+            v = warp_max64((fx[0] != INT64_MIN && c >= ref_k) ? fx[0] : 0);
+          } else {
+            int64_t max_pos = 0;
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) max_pos = max(max_pos, fx[jj]);
+            max_pos = warp_max64(max_pos);
+            for (int bit = 63 - __clzll(max_pos > 0 ? max_pos : 1); bit >= 0; --bit) {
+              const int64_t cand = v | (int64_t(1) << bit);
+              int cnt = 0;
+#pragma unroll
+              for (int jj = 0; jj < NJ; ++jj) cnt += (fx[jj] >= cand) ? 1 : 0;
+              if (warp_sum32(cnt) >= ref_k) v = cand;
+            }
+          }
+        }
+        int c_above = 0;
+        const int64_t hi = v + p.tol_fx, lo = v - p.tol_fx;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) c_above += (fx[jj] != INT64_MIN && fx[jj] > hi) ? 1 : 0;
+        c_above = warp_sum32(c_above);
+        const int k = min(ref_k, nadm);
+        int slots = k - c_above;  // filled from the near-tie group, lowest index first
+        int taken = 0;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) {
+          const bool above = fx[jj] != INT64_MIN && fx[jj] > hi;
+          const bool near = fx[jj] != INT64_MIN && fx[jj] >= lo && fx[jj] <= hi;
+          const uint32_t nb_bal = __ballot_sync(0xffffffffu, near);
+          const int rank = taken + __popc(nb_bal & ((1u << lane) - 1u));
+          const bool pick = above || (near && rank < slots);
+          taken += __popc(nb_bal);
+          const uint32_t bal = __ballot_sync(0xffffffffu, pick);
+          if (lane == jj) sel_word_mine = bal;
+        }
+      } else {
+        sel_word_mine = eq6_step_word<NJ>(fx, key, target, p.tol_fx, lane);
+      }
+      word |= sel_word_mine;
     }
-    word |= sel_word_mine;
   }
   // Readings of this library: sink block 0 and diagonal block q.
   if ((p.flags & 1u) && lane == 0) word |= 1u;
@@ -166,38 +230,96 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
   if (lane == 0) p.counts[row] = cnt;
 }
 
-constexpr int kChunkRows = 256;  // rows per finalize CTA (one per thread)
+constexpr int kChunkRows = kSelectChunkRows;  // rows per finalize CTA (one per thread)
+constexpr int kOrderWarps = kChunkRows / 32;
+
+// Look-back state of the row_ptr scan: one word per chunk of kChunkRows
+// rows (flag in the top two bits: 1 = the chunk's own total, 2 = the total
+// of every row up to and including the chunk), then a ticket counter. It
+// sits after the bitmasks and counts in the workspace and is zeroed by the
+// selection kernel (or, for a finalize-only launch, by a memset) before the
+// finalize kernel runs.
+constexpr uint64_t kLbAggregate = 1ull << 62, kLbInclusive = 2ull << 62, kLbValue = (1ull << 62) - 1;
+
+
+__device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 // Rank the units of one group of (batch, head) slices by cost (listed
 // blocks), heaviest first, ties by unit index, and write their global order:
-// a stable counting sort.
-// Shared memory: cost[units] | start[maxc + 1], maxc = nb * qb_per_unit.
+// a stable counting sort. Warp w places the w-th eighth of the units, after
+// a per-warp histogram gives each warp its first position for every cost.
+// Shared memory: cost[units] | hist[kOrderWarps][maxc + 1] | start[maxc + 1],
+// maxc = nb * qb_per_unit.
 __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
   const int h0 = g * p.group_heads;
   const int gsize = min(p.group_heads, p.bh_count - h0);
   const int units = gsize * p.units_per_bh;
   const int maxc = p.nb * p.qb_per_unit;
+  const int nc = maxc + 1;
   int32_t* cost = sh;
-  int32_t* start = sh + units;
-  for (int c = threadIdx.x; c <= maxc; c += blockDim.x) start[c] = 0;
-  __syncthreads();
-  for (int u = threadIdx.x; u < units; u += blockDim.x) {
-    const int bh = h0 + u / p.units_per_bh, pr = u % p.units_per_bh;
-    int c = 0;
-    for (int j = 0; j < p.qb_per_unit; ++j) {
-      const int qb = pr * p.qb_per_unit + j;
-      if (qb < p.nb) c += p.counts[(int64_t)bh * p.nb + qb];
+  int32_t* hist = sh + units;
+  int32_t* start = hist + kOrderWarps * nc;
+  __shared__ int32_t top_cost;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int c = tid; c < kOrderWarps * nc; c += blockDim.x) hist[c] = 0;
+  if (tid == 0) top_cost = 0;
+  // costs: the listed blocks of the unit's query blocks (at most four);
+  // eight units per thread are loaded before any is used, so the loads of a
+  // thread overlap instead of waiting on each other
+  const int64_t row0 = (int64_t)h0 * p.nb;
+  const int per_unit = p.qb_per_unit;
+  constexpr int kBatch = 8;
+  for (int base = 0; base < units; base += kBatch * (int)blockDim.x) {
+    int c[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int u = base + k * (int)blockDim.x + tid;
+      c[k] = 0;
+      if (u < units) {
+        const int bh = u / p.units_per_bh, pr = u % p.units_per_bh;
+        const int32_t* src = p.counts + row0 + (int64_t)bh * p.nb + pr * per_unit;
+        const int nq = min(per_unit, p.nb - pr * per_unit);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nq) c[k] += __ldg(src + j);
+      }
     }
-    c = min(max(c, 0), maxc);
-    cost[u] = c;
-    atomicAdd(&start[c], 1);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int u = base + k * (int)blockDim.x + tid;
+      if (u < units) cost[u] = min(max(c[k], 0), maxc);
+    }
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 32) {
-    // start[c] = number of units with a larger cost (exclusive scan from the top)
+  const int seg = (units + kOrderWarps - 1) / kOrderWarps;
+  const int u_lo = min(units, warp * seg), u_hi = min(units, u_lo + seg);
+  int my_top = 0;
+  for (int u = u_lo + lane; u < u_hi; u += 32) {
+    atomicAdd(&hist[warp * nc + cost[u]], 1);
+    my_top = max(my_top, cost[u]);
+  }
+  my_top = __reduce_max_sync(0xffffffffu, (uint32_t)my_top);
+  if (lane == 0) atomicMax(&top_cost, my_top);
+  __syncthreads();
+  const int tc = top_cost;
+  // start[c] = number of units with a larger cost (exclusive scan from the top)
+  for (int c = tid; c <= tc; c += blockDim.x) {
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kOrderWarps; ++w) t += hist[w * nc + c];
+    start[c] = t;
+  }
+  __syncthreads();
+  if (warp == 0) {
     int run = 0;
-    for (int top = maxc; top >= 0; top -= 32) {
+    for (int top = tc; top >= 0; top -= 32) {
       const int c = top - lane;
       const int h = (c >= 0) ? start[c] : 0;
       int inc = h;
@@ -209,53 +331,75 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
       if (c >= 0) start[c] = run + inc - h;
       run += __shfl_sync(0xffffffffu, inc, 31);
     }
-    __syncwarp();
-    // place the units in index order, 32 at a time; equal costs keep index order
-    const int64_t gbase = (int64_t)h0 * p.units_per_bh;
-    for (int b = 0; b < units; b += 32) {
-      const int u = b + lane;
-      const int c = (u < units) ? cost[u] : -1;
-      const uint32_t peers = __match_any_sync(0xffffffffu, c);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      const int base = (u < units) ? start[c] : 0;
-      __syncwarp();
-      if (u < units) {
-        p.tile_order[gbase + base + rank] = h0 * p.units_per_bh + u;
-        if (rank == 0) start[c] = base + __popc(peers);
-      }
-      __syncwarp();
+  }
+  __syncthreads();
+  // first position of warp w's units of cost c
+  for (int c = tid; c <= tc; c += blockDim.x) {
+    int run = start[c];
+#pragma unroll
+    for (int w = 0; w < kOrderWarps; ++w) {
+      const int h = hist[w * nc + c];
+      hist[w * nc + c] = run;
+      run += h;
     }
+  }
+  __syncthreads();
+  // place the warp's units in index order, 32 at a time; equal costs keep index order
+  const int64_t gbase = (int64_t)h0 * p.units_per_bh;
+  int32_t* base_w = hist + warp * nc;
+  for (int b = u_lo; b < u_hi; b += 32) {
+    const int u = b + lane;
+    const bool in = u < u_hi;
+    const int c = in ? cost[u] : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, c);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int base = in ? base_w[c] : 0;
+    __syncwarp();
+    if (in) {
+      p.tile_order[gbase + base + rank] = (int32_t)(gbase + u);
+      if (rank == 0) base_w[c] = base + __popc(peers);
+    }
+    __syncwarp();
   }
 }
 
-// Finalize, one launch: CTAs [0, n_chunks) each take kChunkRows rows, add up
-// the counts of every earlier row themselves (no separate scan pass), write
+// Finalize, one launch: the first n_chunks CTAs to start take chunks of
+// kChunkRows rows in the order of their tickets, get the count of all earlier
+// rows from the chunks before them (decoupled look-back: a chunk publishes its
+// own total at once and the running total as soon as it knows it), write
 // their row_ptr entries and emit their rows' column lists in ascending order;
 // the remaining CTAs build the late-step work order, one group each.
-__global__ void __launch_bounds__(kChunkRows) finalize_kernel(const SelectParams p, int n_chunks) {
+__global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectParams p, int n_chunks, uint64_t* lb) {
   extern __shared__ int32_t sh[];
-  __shared__ int64_t red[kChunkRows / 32];
+  __shared__ int32_t red[kOrderWarps];
   __shared__ int32_t start_s[kChunkRows];
+  __shared__ uint32_t s_ticket;
+  __shared__ int64_t s_prefix;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if ((int)blockIdx.x >= n_chunks) {
     order_group(p, blockIdx.x - n_chunks, sh);
     return;
   }
+  uint64_t* state = lb;
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(lb + n_chunks);
+  if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
+  __syncthreads();
+  const int chunk = (int)s_ticket;
   const int64_t rows = (int64_t)p.bh_count * p.nb;
-  const int64_t r0 = (int64_t)blockIdx.x * kChunkRows;
-  // counts of all rows before this chunk
-  int64_t pre = 0;
-  for (int64_t r = tid; r < r0; r += kChunkRows) pre += p.counts[r];
-  pre = warp_sum64(pre);
-  if (lane == 0) red[warp] = pre;
-  __syncthreads();
-  int64_t prefix = 0;
-#pragma unroll
-  for (int w = 0; w < kChunkRows / 32; ++w) prefix += red[w];
-  __syncthreads();
-  // exclusive scan of this chunk's counts
+  const int64_t r0 = (int64_t)chunk * kChunkRows;
+  // Everything this chunk reads is requested first: each thread's row count,
+  // and each warp's rows' bitmask words (warp w emits rows w + 8k; lane j
+  // holds word j). The scan and the look-back then run while they arrive.
+  constexpr int kRowsPerWarp = kChunkRows / kOrderWarps;
   const int64_t r = r0 + tid;
-  const int c = (r < rows) ? p.counts[r] : 0;
+  const int c = (r < rows) ? __ldg(p.counts + r) : 0;
+  uint32_t words[kRowsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k) {
+    const int64_t row = r0 + warp + k * kOrderWarps;
+    words[k] = (row < rows && lane < p.nwords) ? __ldg(p.bits + row * p.nwords + lane) : 0u;
+  }
+  // exclusive scan of this chunk's counts
   int inc = c;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -264,8 +408,45 @@ __global__ void __launch_bounds__(kChunkRows) finalize_kernel(const SelectParams
   }
   if (lane == 31) red[warp] = inc;
   __syncthreads();
-  int64_t wpre = 0;
-  for (int w = 0; w < warp; ++w) wpre += red[w];
+  int wpre = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kOrderWarps; ++w) {
+    wpre += (w < warp) ? red[w] : 0;
+    total += red[w];
+  }
+  if (warp == 0) {
+    // look back over the chunks before this one, 32 at a time
+    if (lane == 0)
+      st_release_gpu(state + chunk, (chunk == 0 ? kLbInclusive : kLbAggregate) | (uint64_t)total);
+    int64_t prefix = 0;
+    int j = chunk - 1;
+    const uint64_t t0 = global_timer_ns();
+    bool timed_out = false;
+    while (j >= 0 && !timed_out) {
+      const int idx = j - lane;
+      uint64_t st = (idx >= 0) ? ld_acquire_gpu(state + idx) : kLbInclusive;
+      // wait until every chunk of this window up to the nearest finished one has published
+      const uint32_t incl = __ballot_sync(0xffffffffu, (st >> 62) == 2u);
+      const int stop = incl ? __ffs(incl) - 1 : 31;  // nearest chunk with a running total
+      const uint32_t unready = __ballot_sync(0xffffffffu, (st >> 62) == 0u) & ((stop == 31) ? 0xffffffffu
+                                                                                   : ((2u << stop) - 1u));
+      if (unready) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) timed_out = true;
+        continue;
+      }
+      int64_t v = (lane <= stop) ? (int64_t)(st & kLbValue) : 0;
+      prefix += warp_sum64(v);
+      if (incl) break;
+      j -= 32;
+    }
+    if (timed_out && lane == 0) atomicOr(p.err, kErrTimeout);
+    if (lane == 0) {
+      if (chunk > 0) st_release_gpu(state + chunk, kLbInclusive | (uint64_t)(prefix + total));
+      s_prefix = prefix;
+    }
+  }
+  __syncthreads();
+  const int64_t prefix = s_prefix;
   const int64_t start = prefix + wpre + inc - c;
   if (r < rows) p.row_ptr[r] = (int32_t)start;
   start_s[tid] = (int32_t)start;
@@ -275,39 +456,45 @@ __global__ void __launch_bounds__(kChunkRows) finalize_kernel(const SelectParams
     if (start + c > p.col_cap) atomicOr(p.err, kErrBadSupport);
   }
   __syncthreads();
-  // emit: one warp per row, lane j holds bitmask word j; a warp's rows are
-  // i = warp + 8k, and all their words are loaded before the first is used
-  // (one round of memory latency instead of one per row)
-  constexpr int kRowsPerWarp = kChunkRows / (kChunkRows / 32);
-  uint32_t words[kRowsPerWarp];
+  // emit, one warp per row (rows past the end hold no bits; a row over
+  // capacity is flagged above)
+  if (p.nwords == 1) {
+    // one word per row: lane i writes key block i if it is set, after the
+    // set bits below it
 #pragma unroll
-  for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int64_t row = r0 + warp + k * (kChunkRows / 32);
-    words[k] = (row < rows && lane < p.nwords) ? __ldg(p.bits + row * p.nwords + lane) : 0u;
-  }
-#pragma unroll
-  for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int i = warp + k * (kChunkRows / 32);
-    const int64_t row = r0 + i;
-    if (row >= rows) break;
-    const uint32_t word = words[k];
-    const int wc = __popc(word);
-    int excl = wc;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, excl, off);
-      if (lane >= off) excl += y;
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int i = warp + k * kOrderWarps;
+      const int64_t st = start_s[i];
+      const uint32_t word = __shfl_sync(0xffffffffu, words[k], 0);
+      if (r0 + i < rows && st + __popc(word) <= p.col_cap && ((word >> lane) & 1u))
+        p.col_idx[st + __popc(word & ((1u << lane) - 1u))] = lane;
     }
-    const int total = __shfl_sync(0xffffffffu, excl, 31);
-    excl -= wc;
-    const int64_t st = start_s[i];
-    if (st + total > p.col_cap) continue;  // flagged above
-    uint32_t w = word;
-    int64_t pos = st + excl;
-    while (w) {
-      const int bit = __ffs(w) - 1;
-      p.col_idx[pos++] = lane * 32 + bit;
-      w &= w - 1;
+  } else {
+    // lane j writes the set bits of word j in order, after the set bits of
+    // the words before it
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int i = warp + k * kOrderWarps;
+      const int64_t st = start_s[i];
+      const uint32_t word = words[k];
+      const int wc = __popc(word);
+      int excl = wc;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, excl, off);
+        if (lane >= off) excl += y;
+      }
+      const int tot = __shfl_sync(0xffffffffu, excl, 31);
+      excl -= wc;
+      if (r0 + i < rows && st + tot <= p.col_cap) {
+        uint32_t w = word;
+        int64_t pos = st + excl;
+        while (w) {
+          const int bit = __ffs(w) - 1;
+          p.col_idx[pos++] = lane * 32 + bit;
+          w &= w - 1;
+        }
+      }
     }
   }
 }
@@ -332,10 +519,10 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   p.units_per_bh = s.units_per_bh;
   p.qb_per_unit = s.qb_per_unit;
   // ranking groups: all slices in one group when its counting sort fits in
-  // shared memory (cost per unit + one counter per cost value)
+  // shared memory (cost per unit + per-warp and total counters per cost value)
   {
     constexpr size_t kOrderSmem = 200u * 1024u;
-    const size_t fixed = ((size_t)s.nb * s.qb_per_unit + 1) * sizeof(int32_t);
+    const size_t fixed = ((size_t)s.nb * s.qb_per_unit + 1) * sizeof(int32_t) * (kOrderWarps + 1);
     const size_t per_slice = (size_t)s.units_per_bh * sizeof(int32_t);
     int64_t g = s.bh_count;
     if (fixed + per_slice * (size_t)g > kOrderSmem) g = (int64_t)((kOrderSmem - fixed) / per_slice);
@@ -347,10 +534,14 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   p.ref_cap = s.ref_cap;
   p.err = s.err;
   const int64_t rows = (int64_t)s.bh_count * s.nb;
+  p.lb = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.bits) + select_lookback_offset(rows, p.nwords));
+  p.lb_words = (int32_t)(select_lookback_bytes(rows) / 8);
   const unsigned grid_rows = (unsigned)((rows + 7) / 8);
   const int rounds = (s.nb + 31) / 32;
   if (s.finalize_only) {
     // the row bitmasks and counts come from the discovery epilogue
+    cudaError_t e = cudaMemsetAsync(p.lb, 0, (size_t)p.lb_words * 8, stream);
+    if (e != cudaSuccess) return e;
   } else if (rounds <= 1) select_rows_kernel<1><<<grid_rows, 256, 0, stream>>>(p);
   else if (rounds <= 2) select_rows_kernel<2><<<grid_rows, 256, 0, stream>>>(p);
   else if (rounds <= 4) select_rows_kernel<4><<<grid_rows, 256, 0, stream>>>(p);
@@ -359,13 +550,15 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   else select_rows_kernel<32><<<grid_rows, 256, 0, stream>>>(p);
   const int n_chunks = (int)((rows + kChunkRows - 1) / kChunkRows);
   const int groups = s.tile_order ? (s.bh_count + p.group_heads - 1) / p.group_heads : 0;
-  const size_t shm =
-      s.tile_order ? ((size_t)p.group_heads * s.units_per_bh + (size_t)s.nb * s.qb_per_unit + 1) * sizeof(int32_t) : 0;
+  const size_t shm = s.tile_order ? ((size_t)p.group_heads * s.units_per_bh +
+                                     (size_t)(kOrderWarps + 1) * ((size_t)s.nb * s.qb_per_unit + 1)) *
+                                        sizeof(int32_t)
+                                  : 0;
   if (shm > 40 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
     if (e != cudaSuccess) return e;
   }
-  finalize_kernel<<<n_chunks + groups, kChunkRows, shm, stream>>>(p, n_chunks);
+  finalize_kernel<<<n_chunks + groups, kChunkRows, shm, stream>>>(p, n_chunks, p.lb);
   return cudaGetLastError();
 }
 

@@ -41,65 +41,47 @@ __device__ __forceinline__ int warp_sum32(int v) {
   return v;
 }
 
-// A mass in the selection's fixed point (round to nearest).
-__device__ __forceinline__ int64_t mass_fx(float m) { return __double2ll_rn((double)m * 4503599627370496.0); }
+// A mass in the selection's fixed point: round(m * 2^52), ties to even, in
+// integer arithmetic on the float's fields (no FP64 work, which is slow on
+// this GPU). With m = M * 2^(e - 150) (M the 24-bit significand), m * 2^52 =
+// M * 2^(e - 98): exact for e >= 98 (masses >= 2^-29), a rounded right
+// shift below. Values past 2^63 saturate; NaN gives 0. Masses are expected
+// in [0, 1].
+__device__ __forceinline__ int64_t mass_fx_bits(uint32_t b) {
+  const uint32_t e = (b >> 23) & 0xffu;
+  const uint32_t frac = b & 0x7fffffu;
+  if (e == 0xffu) return frac ? 0 : ((b >> 31) ? -INT64_MAX : INT64_MAX);
+  const uint32_t sig = e ? (frac | 0x800000u) : frac;
+  const int sh = (int)(e ? e : 1u) - 98;
+  int64_t v;
+  if (sh >= 0) {
+    v = (sh > 39) ? INT64_MAX : (int64_t)((uint64_t)sig << sh);
+  } else {
+    const int r = min(-sh, 26);
+    const uint32_t q = sig >> r, rem = sig & ((1u << r) - 1u), half = 1u << (r - 1);
+    v = (int64_t)(q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u));
+  }
+  return (b >> 31) ? -v : v;
+}
+__device__ __forceinline__ int64_t mass_fx(float m) { return mass_fx_bits(__float_as_uint(m)); }
+
+// Ordering key of a mass for the cut search: its float bits when it is
+// positive (the bits of positive floats order like their values, and
+// mass_fx_bits is non-decreasing in them), 0 otherwise.
+__device__ __forceinline__ uint32_t mass_key(float m) { return (m > 0.f) ? __float_as_uint(m) : 0u; }
 
 // Word `lane` of the row's step support (bit i = key block 32 lane + i) for
-// a positive target mass; tol is the tie tolerance (both fixed point).
-// COMPACT keeps the one-pass loop rolled (a small instruction footprint for
-// callers that share the SM with instruction-heavy warps).
-template <int NJ, bool COMPACT = false>
-__device__ __forceinline__ uint32_t eq6_step_word(const int64_t (&fx)[NJ], int64_t target, int64_t tol, int lane) {
-  int64_t total_pos = 0, max_pos = 0;
-#pragma unroll
-  for (int jj = 0; jj < NJ; ++jj) {
-    total_pos += (fx[jj] > 0) ? fx[jj] : 0;
-    max_pos = max(max_pos, fx[jj]);
-  }
-  total_pos = warp_sum64(total_pos);
-  max_pos = warp_max64(max_pos);
+// a positive target mass; tol is the tie tolerance (both fixed point). fx
+// holds the fixed-point masses (INT64_MIN past the admissible range).
+//
+// v* (the k-th mass) is the fixed-point value at which the cumulative mass,
+// taken in descending order, first reaches the target: the largest v with
+// sum{fx >= v} >= target. The callers find v* (eq6_cut_value below); this
+// part forms the support from it.
+template <int NJ>
+__device__ __forceinline__ uint32_t eq6_word_from_cut(const int64_t (&fx)[NJ], int64_t v, int64_t target,
+                                                      int64_t tol, int lane) {
   uint32_t sel_word_mine = 0;  // the word this lane will hold (word index = lane)
-  if (total_pos < target) {
-    // Eq 6 cannot reach the target: every admissible block.
-#pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) {
-      const uint32_t bal = __ballot_sync(0xffffffffu, fx[jj] != INT64_MIN);
-      if (lane == jj) sel_word_mine = bal;
-    }
-    return sel_word_mine;
-  }
-  // largest v with sum_{fx >= v} fx >= target (v > 0 since target > 0);
-  // v <= the largest mass, so bits above its top bit stay zero
-  int64_t v = 0;
-  if (NJ == 1) {
-    // one value per lane: v = the largest value x with sum{>= x} >= target
-    // (the value the bitwise search below converges to)
-    const int64_t mine = fx[0];
-    int64_t acc = 0;
-    if (COMPACT) {
-#pragma unroll 1
-      for (int j = 0; j < 32; ++j) {
-        const int64_t o = __shfl_sync(0xffffffffu, mine, j);
-        acc += (o >= mine && o > 0) ? o : 0;
-      }
-    } else {
-#pragma unroll 8
-      for (int j = 0; j < 32; ++j) {
-        const int64_t o = __shfl_sync(0xffffffffu, mine, j);
-        acc += (o >= mine && o > 0) ? o : 0;
-      }
-    }
-    v = warp_max64((mine > 0 && acc >= target) ? mine : 0);
-  } else {
-    for (int bit = 63 - __clzll(max_pos); bit >= 0; --bit) {
-      const int64_t cand = v | (int64_t(1) << bit);
-      int64_t sacc = 0;
-#pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
-      sacc = warp_sum_u63(sacc);
-      if (sacc >= target) v = cand;
-    }
-  }
   int64_t s_gt = 0;
   int c_gt = 0, c_above = 0;
   const int64_t hi = v + tol, lo = v - tol;
@@ -109,11 +91,16 @@ __device__ __forceinline__ uint32_t eq6_step_word(const int64_t (&fx)[NJ], int64
     c_gt += (fx[jj] > v) ? 1 : 0;
     c_above += (fx[jj] > hi) ? 1 : 0;
   }
-  s_gt = warp_sum64(s_gt);
-  c_gt = warp_sum32(c_gt);
-  c_above = warp_sum32(c_above);
+  s_gt = warp_sum_u63(s_gt);
+  c_gt = (int)__reduce_add_sync(0xffffffffu, (uint32_t)c_gt);
+  c_above = (int)__reduce_add_sync(0xffffffffu, (uint32_t)c_above);
+  // m = ceil(need / v) blocks of mass v complete the target; 1 <= m <= the
+  // number of blocks at v (usually 1), so an estimate corrected by exact
+  // integer products replaces a 64-bit division
   const int64_t need = target - s_gt;  // > 0
-  const int m = (int)((need + v - 1) / v);
+  int m = (int)fminf(fmaxf((float)need / (float)v, 1.f), 4096.f);
+  while (m > 1 && (int64_t)(m - 1) * v >= need) --m;
+  while ((int64_t)m * v < need) ++m;
   const int k = c_gt + m;
   const int slots = k - c_above;  // filled from the near-tie group, lowest index first
   int taken = 0;
@@ -130,6 +117,136 @@ __device__ __forceinline__ uint32_t eq6_step_word(const int64_t (&fx)[NJ], int64
     if (lane == jj) sel_word_mine = bal;
   }
   return sel_word_mine;
+}
+
+// Every admissible block (Eq 6 cannot reach the target).
+template <int NJ>
+__device__ __forceinline__ uint32_t eq6_all_admissible(const int64_t (&fx)[NJ], int lane) {
+  uint32_t sel_word_mine = 0;
+#pragma unroll
+  for (int jj = 0; jj < NJ; ++jj) {
+    const uint32_t bal = __ballot_sync(0xffffffffu, fx[jj] != INT64_MIN);
+    if (lane == jj) sel_word_mine = bal;
+  }
+  return sel_word_mine;
+}
+
+// v* for rows of up to 32 blocks (one value per lane): each lane sums the
+// masses >= its own.
+template <bool COMPACT>
+__device__ __forceinline__ int64_t eq6_cut_one_round(int64_t mine, int64_t target) {
+  int64_t acc = 0;
+  if (COMPACT) {
+#pragma unroll 1
+    for (int j = 0; j < 32; ++j) {
+      const int64_t o = __shfl_sync(0xffffffffu, mine, j);
+      acc += (o >= mine && o > 0) ? o : 0;
+    }
+  } else {
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+      const int64_t o = __shfl_sync(0xffffffffu, mine, j);
+      acc += (o >= mine && o > 0) ? o : 0;
+    }
+  }
+  return warp_max64((mine > 0 && acc >= target) ? mine : 0);
+}
+
+// The selection kernel's step: key holds the masses' ordering keys (mass_key;
+// 0 past the admissible range). Rows of more than 32 blocks take the
+// distinct largest keys one at a time (a warp max and a warp count per
+// value), which ends after a few values on the concentrated rows the method
+// produces; after kExtractLimit values without reaching the target, a
+// bitwise search over the 31-bit keys finds the crossing instead
+// (K* = the largest key K with sum{key >= K} fx >= target; since fx is
+// non-decreasing in the key, v* = fx(K*)).
+constexpr int kExtractLimit = 24;
+
+template <int NJ>
+__device__ __forceinline__ uint32_t eq6_step_word(const int64_t (&fx)[NJ], const uint32_t (&key)[NJ],
+                                                  int64_t target, int64_t tol, int lane) {
+  int64_t total_pos = 0;
+  uint32_t kmax = 0u;
+#pragma unroll
+  for (int jj = 0; jj < NJ; ++jj) {
+    total_pos += (fx[jj] > 0) ? fx[jj] : 0;
+    kmax = max(kmax, key[jj]);
+  }
+  if (warp_sum_u63(total_pos) < target) return eq6_all_admissible<NJ>(fx, lane);
+  int64_t v = 0;  // > 0 since target > 0
+  if (NJ == 1) {
+    v = eq6_cut_one_round<false>(fx[0], target);
+  } else {
+    uint32_t rem[NJ];
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) rem[jj] = key[jj];
+    uint32_t top = __reduce_max_sync(0xffffffffu, kmax);
+    const uint32_t kmax_all = top;
+    int64_t cum = 0;
+    bool found = false;
+#pragma unroll 1
+    for (int it = 0; it < kExtractLimit && top != 0u; ++it) {
+      uint32_t c = 0u, nxt = 0u;
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) {
+        const bool hit = rem[jj] == top;
+        c += hit ? 1u : 0u;
+        rem[jj] = hit ? 0u : rem[jj];
+        nxt = max(nxt, rem[jj]);
+      }
+      c = __reduce_add_sync(0xffffffffu, c);
+      const int64_t f = mass_fx_bits(top);
+      cum += (int64_t)c * f;
+      if (cum >= target) {
+        v = f;
+        found = true;
+        break;
+      }
+      top = __reduce_max_sync(0xffffffffu, nxt);
+    }
+    if (!found) {
+      uint32_t kk = 0u;
+      for (int bit = 31 - __clz(kmax_all); bit >= 0; --bit) {
+        const uint32_t cand = kk | (1u << bit);
+        int64_t sacc = 0;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) sacc += (key[jj] >= cand) ? fx[jj] : 0;
+        if (warp_sum_u63(sacc) >= target) kk = cand;
+      }
+      v = mass_fx_bits(kk);
+    }
+  }
+  return eq6_word_from_cut<NJ>(fx, v, target, tol, lane);
+}
+
+// The same step with a small footprint, for the discovery epilogue that
+// selects while it writes the masses (its warps share the SM with
+// instruction-heavy warps and run with few registers): the loops stay
+// rolled and v* comes from a bitwise search over the fixed-point values.
+template <int NJ>
+__device__ __forceinline__ uint32_t eq6_step_word_compact(const int64_t (&fx)[NJ], int64_t target, int64_t tol,
+                                                          int lane) {
+  int64_t total_pos = 0, max_pos = 0;
+#pragma unroll
+  for (int jj = 0; jj < NJ; ++jj) {
+    total_pos += (fx[jj] > 0) ? fx[jj] : 0;
+    max_pos = max(max_pos, fx[jj]);
+  }
+  if (warp_sum_u63(total_pos) < target) return eq6_all_admissible<NJ>(fx, lane);
+  int64_t v = 0;
+  if (NJ == 1) {
+    v = eq6_cut_one_round<true>(fx[0], target);
+  } else {
+    max_pos = warp_max64(max_pos);
+    for (int bit = 63 - __clzll(max_pos); bit >= 0; --bit) {
+      const int64_t cand = v | (int64_t(1) << bit);
+      int64_t sacc = 0;
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) sacc += (fx[jj] >= cand) ? fx[jj] : 0;
+      if (warp_sum_u63(sacc) >= target) v = cand;
+    }
+  }
+  return eq6_word_from_cut<NJ>(fx, v, target, tol, lane);
 }
 
 }  // namespace wise

@@ -284,7 +284,7 @@ size_t wise_select_workspace(const wise_attn_desc* desc, int32_t window) {
   const Shape s = shape_of(desc);
   const int64_t rows = s.bh * s.nb;
   const int64_t words = (s.nb + 31) / 32;
-  return (size_t)(rows * words * 4 + rows * 4 + 256);
+  return (size_t)(select_lookback_offset(rows, words) + select_lookback_bytes(rows) + 256);
 }
 
 int wise_attn_discover(const wise_attn_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,

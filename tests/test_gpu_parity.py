@@ -153,7 +153,8 @@ def _check_tile_order(sup):
     # first, ties by unit index.
     qpu = 128 // sup.block
     nb = sup.seq_len // sup.block
-    if (units + nb * qpu + 1) * 4 <= 200 * 1024:
+    # the ranking CTA holds one cost per unit and nine counters per cost value
+    if (units + 9 * (nb * qpu + 1)) * 4 <= 200 * 1024:
         counts = np.diff(sup.row_ptr.cpu().numpy().astype(np.int64)).reshape(sup.batch * sup.heads, nb)
         tiles = units // (sup.batch * sup.heads)
         pad = np.zeros((sup.batch * sup.heads, tiles * qpu), np.int64)
@@ -161,6 +162,39 @@ def _check_tile_order(sup):
         cost = pad.reshape(sup.batch * sup.heads, tiles, qpu).sum(-1).reshape(-1)
         expect = np.argsort(-cost, kind="stable")
         assert np.array_equal(order, expect)
+
+
+def _tiny_mass_rows(nb, seed, lo_exp, hi_exp):
+    """One head whose rows hold mass 0.5 in block 0 and masses between
+    2^lo_exp and 2^hi_exp (below 2^-29, where the 2^-52 fixed point of Eq 6's
+    cumulative sum rounds) elsewhere, a few of them exactly halfway between
+    two fixed-point steps, (2j + 1) * 2^-53, where rounding goes to even."""
+    rng = np.random.default_rng(seed)
+    m = np.zeros((1, 1, 1, nb, nb), np.float32)
+    for q in range(nb):
+        r = np.exp2(rng.uniform(lo_exp, hi_exp, q + 1)).astype(np.float32)
+        halfway = rng.random(q + 1) < 0.2
+        r[halfway] = ((2 * rng.integers(1, 1 << (hi_exp + 52), halfway.sum()) + 1) * 2.0 ** -53).astype(np.float32)
+        r[0] = 0.5
+        m[0, 0, 0, q, :q + 1] = r
+    return m
+
+
+@pytest.mark.parametrize("nb", [20, 40, 300])
+@pytest.mark.parametrize("lo_exp,hi_exp,eta", [(-36, -30, 0.5 + 2.0 ** -31), (-40, -36, 0.5 + 2.0 ** -32)])
+def test_select_bit_exact_where_the_fixed_point_rounds(nb, lo_exp, hi_exp, eta):
+    """The cut falls among masses the 2^-52 fixed point rounds (ties to
+    even): the number of blocks Eq 6 takes depends on every one of them, so
+    any difference in the rounding between the kernel and the oracle changes
+    the CSR. The second range needs more than 24 values to reach eta, which
+    takes the kernel's search path instead of its one-value-at-a-time path."""
+    m = _tiny_mass_rows(nb, seed=100 * nb - lo_exp, lo_exp=lo_exp, hi_exp=hi_exp)
+    sup = wise.select_support(torch.from_numpy(m).cuda(), nb * 64, 64, 64, eta, 0)
+    wise.check_device()
+    rp_ref, ci_ref = O.select(m.astype(np.float64), eta, 0)
+    rp = sup.row_ptr.cpu().numpy()
+    assert np.array_equal(rp, rp_ref)
+    assert np.array_equal(sup.col_idx.cpu().numpy()[:rp[-1]], ci_ref)
 
 
 def test_select_on_gpu_masses_matches_oracle_select():

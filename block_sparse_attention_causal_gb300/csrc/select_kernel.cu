@@ -58,61 +58,96 @@ struct SelectParams {
   uint32_t* err;
 };
 
-// Word `lane` of the union over the window of one row's Eq 6 step supports,
-// with NJ rounds of 32 blocks covering the row's q + 1 admissible blocks.
-// The next step's masses are loaded while the current step is selected.
+// Word `lane` of one row's Eq 6 step support at window step w, with NJ rounds
+// of 32 blocks covering the row's q + 1 admissible blocks.
 template <int NJ>
-__device__ __forceinline__ uint32_t union_eq6(const SelectParams& p, int bh, int q, int lane) {
+__device__ __forceinline__ uint32_t step_eq6(const SelectParams& p, int bh, int q, int w, int lane) {
   const int nadm = q + 1;
-  auto src = [&](int w) { return p.mass + (((int64_t)w * p.bh_count + bh) * p.nb + q) * p.nb; };
-  float cur[NJ], nxt[NJ];
+  const float* src = p.mass + (((int64_t)w * p.bh_count + bh) * p.nb + q) * p.nb;
+  float m[NJ];
 #pragma unroll
   for (int jj = 0; jj < NJ; ++jj) {
     const int b = jj * 32 + lane;  // coalesced load order: jj-major
-    cur[jj] = (b < nadm) ? __ldg(src(0) + b) : 0.f;
+    m[jj] = (b < nadm) ? __ldg(src + b) : 0.f;
   }
-  uint32_t word = 0;
-  for (int w = 0; w < p.window; ++w) {
-    if (w + 1 < p.window) {
+  int64_t fx[NJ];
+  uint32_t key[NJ];
+  // every admissible mass of the row in [2^-29, 2^10) (the usual case): the
+  // fixed point is a plain shift; otherwise the general rounding
+  bool exact = true;
 #pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) {
-        const int b = jj * 32 + lane;
-        nxt[jj] = (b < nadm) ? __ldg(src(w + 1) + b) : 0.f;
-      }
-    }
-    int64_t fx[NJ];
-    uint32_t key[NJ];
+  for (int jj = 0; jj < NJ; ++jj)
+    exact &= (jj * 32 + lane >= nadm) || mass_fx_exact(__float_as_uint(m[jj]));
+  if (__all_sync(0xffffffffu, exact)) {
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) {
       const bool adm = jj * 32 + lane < nadm;
-      fx[jj] = adm ? mass_fx(cur[jj]) : INT64_MIN;
-      key[jj] = adm ? mass_key(cur[jj]) : 0u;
+      const uint32_t b = __float_as_uint(m[jj]);
+      fx[jj] = adm ? mass_fx_exact_bits(b) : INT64_MIN;
+      key[jj] = adm ? b : 0u;
     }
-    word |= eq6_step_word<NJ>(fx, key, p.target_fx, p.tol_fx, lane);
+  } else {
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) cur[jj] = nxt[jj];
+    for (int jj = 0; jj < NJ; ++jj) {
+      const bool adm = jj * 32 + lane < nadm;
+      fx[jj] = adm ? mass_fx(m[jj]) : INT64_MIN;
+      key[jj] = adm ? mass_key(m[jj]) : 0u;
+    }
   }
-  return word;
+  return eq6_step_word<NJ>(fx, key, p.target_fx, p.tol_fx, lane);
 }
 
-// The Eq 6 union of one row with the fewest rounds that cover its q + 1
-// admissible blocks (a row near the start of the sequence costs less than
-// one near its end).
+// The same with the fewest rounds that cover the row (a row near the start
+// of the sequence costs less than one near its end).
 template <int NJ>
-__device__ __forceinline__ uint32_t union_eq6_any(const SelectParams& p, int bh, int q, int lane) {
+__device__ __forceinline__ uint32_t step_eq6_any(const SelectParams& p, int bh, int q, int w, int lane) {
   const int nadm = q + 1;
-  if (NJ == 1 || nadm <= 32) return union_eq6<1>(p, bh, q, lane);
-  if (NJ == 2 || nadm <= 64) return union_eq6<(NJ < 2 ? NJ : 2)>(p, bh, q, lane);
-  if (NJ == 4 || nadm <= 128) return union_eq6<(NJ < 4 ? NJ : 4)>(p, bh, q, lane);
-  if (NJ == 8 || nadm <= 256) return union_eq6<(NJ < 8 ? NJ : 8)>(p, bh, q, lane);
-  if (NJ == 16 || nadm <= 512) return union_eq6<(NJ < 16 ? NJ : 16)>(p, bh, q, lane);
-  return union_eq6<NJ>(p, bh, q, lane);
+  if (NJ == 1 || nadm <= 32) return step_eq6<1>(p, bh, q, w, lane);
+  if (NJ == 2 || nadm <= 64) return step_eq6<(NJ < 2 ? NJ : 2)>(p, bh, q, w, lane);
+  if (NJ == 4 || nadm <= 128) return step_eq6<(NJ < 4 ? NJ : 4)>(p, bh, q, w, lane);
+  if (NJ == 8 || nadm <= 256) return step_eq6<(NJ < 8 ? NJ : 8)>(p, bh, q, w, lane);
+  if (NJ == 16 || nadm <= 512) return step_eq6<(NJ < 16 ? NJ : 16)>(p, bh, q, w, lane);
+  return step_eq6<NJ>(p, bh, q, w, lane);
 }
 
-// 8 warps per CTA, one row per warp; NJ rounds of 32 blocks cover nb <= 32 NJ.
-// Up to 8 rounds the registers are capped so that four CTAs share an SM.
+// Eq 6 over the window: one warp per (row, window step), window warps per
+// row, rows_per_cta rows per CTA. Each warp ORs its step support into the
+// row's words in shared memory; the row's step-0 warp then adds the sink /
+// diagonal blocks and writes the row's bitmask and count.
 template <int NJ>
-__global__ void __launch_bounds__(256, (NJ <= 8) ? 4 : 1) select_rows_kernel(const SelectParams p) {
+__global__ void __launch_bounds__(256, (NJ <= 8) ? 4 : 1) select_steps_kernel(const SelectParams p, int rows_per_cta) {
+  __shared__ uint32_t rowbits[8][32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  // the finalize kernel that follows starts from a cleared look-back state
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.lb_words; i += blockDim.x) p.lb[i] = 0ull;
+  const int r_local = wid / p.window, w = wid % p.window;
+  const int64_t row = (int64_t)blockIdx.x * rows_per_cta + r_local;
+  const int64_t rows = (int64_t)p.bh_count * p.nb;
+  const bool live = r_local < rows_per_cta && row < rows;
+  if (w == 0 && r_local < rows_per_cta) rowbits[r_local][lane] = 0u;
+  __syncthreads();
+  const int bh = live ? (int)(row / p.nb) : 0;
+  const int q = live ? (int)(row % p.nb) : 0;
+  if (live) {
+    const uint32_t word = step_eq6_any<NJ>(p, bh, q, w, lane);
+    if (word) atomicOr(&rowbits[r_local][lane], word);
+  }
+  __syncthreads();
+  if (!live || w != 0) return;
+  uint32_t word = rowbits[r_local][lane];
+  // Readings of this library: sink block 0 and diagonal block q.
+  if ((p.flags & 1u) && lane == 0) word |= 1u;
+  if ((p.flags & 2u) && lane == (q >> 5)) word |= 1u << (q & 31);
+  const int cnt = warp_sum32(__popc(word));
+  if (lane < p.nwords) p.bits[row * p.nwords + lane] = word;
+  if (lane == 0) p.counts[row] = cnt;
+}
+
+// The early-static controls (one step, window 1): 8 warps per CTA, one row
+// per warp; NJ rounds of 32 blocks cover nb <= 32 NJ.
+template <int NJ>
+__global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) {
   __shared__ uint32_t refbits[8][32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   // the finalize kernel that follows starts from a cleared look-back state
@@ -125,9 +160,7 @@ __global__ void __launch_bounds__(256, (NJ <= 8) ? 4 : 1) select_rows_kernel(con
   const int q = (int)(row % p.nb);
   const int nadm = q + 1;  // admissible key blocks 0..q
   uint32_t word = 0;  // word `lane` of the row's union bitmask
-  if (p.mode == 0) {
-    word = union_eq6_any<NJ>(p, bh, q, lane);
-  } else {
+  {
     // Controls: the reference row as a bitmask (entries outside 0..q flagged
     // and skipped; repeated entries count once); in_ref[jj] is this lane's
     // block.
@@ -270,31 +303,27 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int c = tid; c < kOrderWarps * nc; c += blockDim.x) hist[c] = 0;
   if (tid == 0) top_cost = 0;
-  // costs: the listed blocks of the unit's query blocks (at most four);
-  // eight units per thread are loaded before any is used, so the loads of a
-  // thread overlap instead of waiting on each other
+  // costs: the listed blocks of the unit's query blocks (at most four); the
+  // counts of kBatch units per thread are all requested before any is used,
+  // so a thread's loads overlap instead of waiting on each other
   const int64_t row0 = (int64_t)h0 * p.nb;
   const int per_unit = p.qb_per_unit;
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 16;
   for (int base = 0; base < units; base += kBatch * (int)blockDim.x) {
-    int c[kBatch];
+    int v[kBatch][4];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const int u = base + k * (int)blockDim.x + tid;
-      c[k] = 0;
-      if (u < units) {
-        const int bh = u / p.units_per_bh, pr = u % p.units_per_bh;
-        const int32_t* src = p.counts + row0 + (int64_t)bh * p.nb + pr * per_unit;
-        const int nq = min(per_unit, p.nb - pr * per_unit);
+      const int bh = u / p.units_per_bh, pr = u % p.units_per_bh;
+      const int nq = (u < units) ? min(per_unit, p.nb - pr * per_unit) : 0;
+      const int32_t* src = p.counts + row0 + (int64_t)bh * p.nb + pr * per_unit;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (j < nq) c[k] += __ldg(src + j);
-      }
+      for (int j = 0; j < 4; ++j) v[k][j] = (j < nq) ? __ldg(src + j) : 0;
     }
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const int u = base + k * (int)blockDim.x + tid;
-      if (u < units) cost[u] = min(max(c[k], 0), maxc);
+      if (u < units) cost[u] = min(max(v[k][0] + v[k][1] + v[k][2] + v[k][3], 0), maxc);
     }
   }
   __syncthreads();
@@ -373,6 +402,7 @@ __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectPar
   extern __shared__ int32_t sh[];
   __shared__ int32_t red[kOrderWarps];
   __shared__ int32_t start_s[kChunkRows];
+  __shared__ int32_t cnt_s[kChunkRows];
   __shared__ uint32_t s_ticket;
   __shared__ int64_t s_prefix;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -387,18 +417,9 @@ __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectPar
   const int chunk = (int)s_ticket;
   const int64_t rows = (int64_t)p.bh_count * p.nb;
   const int64_t r0 = (int64_t)chunk * kChunkRows;
-  // Everything this chunk reads is requested first: each thread's row count,
-  // and each warp's rows' bitmask words (warp w emits rows w + 8k; lane j
-  // holds word j). The scan and the look-back then run while they arrive.
-  constexpr int kRowsPerWarp = kChunkRows / kOrderWarps;
   const int64_t r = r0 + tid;
   const int c = (r < rows) ? __ldg(p.counts + r) : 0;
-  uint32_t words[kRowsPerWarp];
-#pragma unroll
-  for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int64_t row = r0 + warp + k * kOrderWarps;
-    words[k] = (row < rows && lane < p.nwords) ? __ldg(p.bits + row * p.nwords + lane) : 0u;
-  }
+  cnt_s[tid] = c;
   // exclusive scan of this chunk's counts
   int inc = c;
 #pragma unroll
@@ -456,43 +477,29 @@ __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectPar
     if (start + c > p.col_cap) atomicOr(p.err, kErrBadSupport);
   }
   __syncthreads();
-  // emit, one warp per row (rows past the end hold no bits; a row over
-  // capacity is flagged above)
-  if (p.nwords == 1) {
-    // one word per row: lane i writes key block i if it is set, after the
-    // set bits below it
+  // emit, one lane per row: lane l of warp w writes row w + 8 l, its set
+  // bits in ascending order from the row's start (rows past the end hold no
+  // bits; a row over capacity is flagged above)
+  {
+    const int i = warp + kOrderWarps * lane;
+    const int64_t row = r0 + i;
+    if (row < rows) {
+      int64_t pos = start_s[i];
+      const int64_t end = pos + cnt_s[i];
+      if (end <= p.col_cap) {
+        const uint32_t* wp = p.bits + row * p.nwords;
+        for (int w0 = 0; w0 < p.nwords; w0 += 8) {
+          uint32_t rw[8];
 #pragma unroll
-    for (int k = 0; k < kRowsPerWarp; ++k) {
-      const int i = warp + k * kOrderWarps;
-      const int64_t st = start_s[i];
-      const uint32_t word = __shfl_sync(0xffffffffu, words[k], 0);
-      if (r0 + i < rows && st + __popc(word) <= p.col_cap && ((word >> lane) & 1u))
-        p.col_idx[st + __popc(word & ((1u << lane) - 1u))] = lane;
-    }
-  } else {
-    // lane j writes the set bits of word j in order, after the set bits of
-    // the words before it
+          for (int j = 0; j < 8; ++j) rw[j] = (w0 + j < p.nwords) ? __ldg(wp + w0 + j) : 0u;
 #pragma unroll
-    for (int k = 0; k < kRowsPerWarp; ++k) {
-      const int i = warp + k * kOrderWarps;
-      const int64_t st = start_s[i];
-      const uint32_t word = words[k];
-      const int wc = __popc(word);
-      int excl = wc;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, excl, off);
-        if (lane >= off) excl += y;
-      }
-      const int tot = __shfl_sync(0xffffffffu, excl, 31);
-      excl -= wc;
-      if (r0 + i < rows && st + tot <= p.col_cap) {
-        uint32_t w = word;
-        int64_t pos = st + excl;
-        while (w) {
-          const int bit = __ffs(w) - 1;
-          p.col_idx[pos++] = lane * 32 + bit;
-          w &= w - 1;
+          for (int j = 0; j < 8; ++j) {
+            uint32_t x = rw[j];
+            while (x && pos < end) {
+              p.col_idx[pos++] = 32 * (w0 + j) + __ffs(x) - 1;
+              x &= x - 1;
+            }
+          }
         }
       }
     }
@@ -538,10 +545,21 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   p.lb_words = (int32_t)(select_lookback_bytes(rows) / 8);
   const unsigned grid_rows = (unsigned)((rows + 7) / 8);
   const int rounds = (s.nb + 31) / 32;
+  // Eq 6: window warps per row, as many rows per CTA as fit in 8 warps
+  const int rpc = (s.window >= 1 && s.window <= 8) ? 8 / s.window : 1;
+  const unsigned grid_steps = (unsigned)((rows + rpc - 1) / rpc);
+  const unsigned threads_steps = (unsigned)(32 * s.window * rpc);
   if (s.finalize_only) {
     // the row bitmasks and counts come from the discovery epilogue
     cudaError_t e = cudaMemsetAsync(p.lb, 0, (size_t)p.lb_words * 8, stream);
     if (e != cudaSuccess) return e;
+  } else if (s.mode == 0) {
+    if (rounds <= 1) select_steps_kernel<1><<<grid_steps, threads_steps, 0, stream>>>(p, rpc);
+    else if (rounds <= 2) select_steps_kernel<2><<<grid_steps, threads_steps, 0, stream>>>(p, rpc);
+    else if (rounds <= 4) select_steps_kernel<4><<<grid_steps, threads_steps, 0, stream>>>(p, rpc);
+    else if (rounds <= 8) select_steps_kernel<8><<<grid_steps, threads_steps, 0, stream>>>(p, rpc);
+    else if (rounds <= 16) select_steps_kernel<16><<<grid_steps, threads_steps, 0, stream>>>(p, rpc);
+    else select_steps_kernel<32><<<grid_steps, threads_steps, 0, stream>>>(p, rpc);
   } else if (rounds <= 1) select_rows_kernel<1><<<grid_rows, 256, 0, stream>>>(p);
   else if (rounds <= 2) select_rows_kernel<2><<<grid_rows, 256, 0, stream>>>(p);
   else if (rounds <= 4) select_rows_kernel<4><<<grid_rows, 256, 0, stream>>>(p);

@@ -65,6 +65,13 @@ __device__ __forceinline__ int64_t mass_fx_bits(uint32_t b) {
 }
 __device__ __forceinline__ int64_t mass_fx(float m) { return mass_fx_bits(__float_as_uint(m)); }
 
+// Whether mass_fx_bits is the plain shift M << (e - 98) for this float: a
+// positive mass in [2^-29, 2^10), where the fixed point is exact.
+__device__ __forceinline__ bool mass_fx_exact(uint32_t b) { return b >= (98u << 23) && b < (137u << 23); }
+__device__ __forceinline__ int64_t mass_fx_exact_bits(uint32_t b) {
+  return (int64_t)((uint64_t)((b & 0x7fffffu) | 0x800000u) << ((b >> 23) - 98u));
+}
+
 // Ordering key of a mass for the cut search: its float bits when it is
 // positive (the bits of positive floats order like their values, and
 // mass_fx_bits is non-decreasing in them), 0 otherwise.
@@ -80,20 +87,27 @@ __device__ __forceinline__ uint32_t mass_key(float m) { return (m > 0.f) ? __flo
 // part forms the support from it.
 template <int NJ>
 __device__ __forceinline__ uint32_t eq6_word_from_cut(const int64_t (&fx)[NJ], int64_t v, int64_t target,
-                                                      int64_t tol, int lane) {
+                                                      int64_t tol, int lane, bool gt_known = false,
+                                                      int64_t s_gt_known = 0, int c_gt_known = 0) {
   uint32_t sel_word_mine = 0;  // the word this lane will hold (word index = lane)
-  int64_t s_gt = 0;
-  int c_gt = 0, c_above = 0;
   const int64_t hi = v + tol, lo = v - tol;
+  int64_t s_gt = s_gt_known;
+  int c_gt = c_gt_known, c_above = 0, c_near = 0;
 #pragma unroll
   for (int jj = 0; jj < NJ; ++jj) {
-    s_gt += (fx[jj] > v) ? fx[jj] : 0;
-    c_gt += (fx[jj] > v) ? 1 : 0;
+    if (!gt_known) {
+      s_gt += (fx[jj] > v) ? fx[jj] : 0;
+      c_gt += (fx[jj] > v) ? 1 : 0;
+    }
     c_above += (fx[jj] > hi) ? 1 : 0;
+    c_near += (fx[jj] != INT64_MIN && fx[jj] >= lo && fx[jj] <= hi) ? 1 : 0;
   }
-  s_gt = warp_sum_u63(s_gt);
-  c_gt = (int)__reduce_add_sync(0xffffffffu, (uint32_t)c_gt);
+  if (!gt_known) {
+    s_gt = warp_sum_u63(s_gt);
+    c_gt = (int)__reduce_add_sync(0xffffffffu, (uint32_t)c_gt);
+  }
   c_above = (int)__reduce_add_sync(0xffffffffu, (uint32_t)c_above);
+  c_near = (int)__reduce_add_sync(0xffffffffu, (uint32_t)c_near);
   // m = ceil(need / v) blocks of mass v complete the target; 1 <= m <= the
   // number of blocks at v (usually 1), so an estimate corrected by exact
   // integer products replaces a 64-bit division
@@ -103,6 +117,16 @@ __device__ __forceinline__ uint32_t eq6_word_from_cut(const int64_t (&fx)[NJ], i
   while ((int64_t)m * v < need) ++m;
   const int k = c_gt + m;
   const int slots = k - c_above;  // filled from the near-tie group, lowest index first
+  if (slots >= c_near) {
+    // the whole near-tie group is taken (the usual case: v alone)
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) {
+      const bool pick = fx[jj] != INT64_MIN && fx[jj] >= lo;
+      const uint32_t bal = __ballot_sync(0xffffffffu, pick);
+      if (lane == jj) sel_word_mine = bal;
+    }
+    return sel_word_mine;
+  }
   int taken = 0;
 #pragma unroll
   for (int jj = 0; jj < NJ; ++jj) {
@@ -162,61 +186,76 @@ __device__ __forceinline__ int64_t eq6_cut_one_round(int64_t mine, int64_t targe
 // non-decreasing in the key, v* = fx(K*)).
 constexpr int kExtractLimit = 24;
 
+// Compare-exchange keeping a >= b.
+__device__ __forceinline__ void cx_desc(uint32_t& a, uint32_t& b) {
+  const uint32_t hi = max(a, b), lo = min(a, b);
+  a = hi;
+  b = lo;
+}
+// Each lane's keys in descending order (a sorting network).
+template <int NJ>
+__device__ __forceinline__ void sort_desc(uint32_t (&q)[NJ]) {
+#pragma unroll
+  for (int k = 2; k <= NJ; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+      for (int i = 0; i < NJ; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          if ((i & k) == 0) cx_desc(q[i], q[l]);
+          else cx_desc(q[l], q[i]);
+        }
+      }
+}
+
 template <int NJ>
 __device__ __forceinline__ uint32_t eq6_step_word(const int64_t (&fx)[NJ], const uint32_t (&key)[NJ],
                                                   int64_t target, int64_t tol, int lane) {
   int64_t total_pos = 0;
-  uint32_t kmax = 0u;
 #pragma unroll
-  for (int jj = 0; jj < NJ; ++jj) {
-    total_pos += (fx[jj] > 0) ? fx[jj] : 0;
-    kmax = max(kmax, key[jj]);
-  }
+  for (int jj = 0; jj < NJ; ++jj) total_pos += (fx[jj] > 0) ? fx[jj] : 0;
   if (warp_sum_u63(total_pos) < target) return eq6_all_admissible<NJ>(fx, lane);
-  int64_t v = 0;  // > 0 since target > 0
-  if (NJ == 1) {
-    v = eq6_cut_one_round<false>(fx[0], target);
-  } else {
-    uint32_t rem[NJ];
+  if (NJ == 1) return eq6_word_from_cut<NJ>(fx, eq6_cut_one_round<false>(fx[0], target), target, tol, lane);
+  // the lane's keys in descending order: its largest remaining one is q[0]
+  uint32_t q[NJ];
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) rem[jj] = key[jj];
-    uint32_t top = __reduce_max_sync(0xffffffffu, kmax);
-    const uint32_t kmax_all = top;
-    int64_t cum = 0;
-    bool found = false;
+  for (int jj = 0; jj < NJ; ++jj) q[jj] = key[jj];
+  sort_desc<NJ>(q);
+  const uint32_t kmax_all = __reduce_max_sync(0xffffffffu, q[0]);
+  uint32_t top = kmax_all;
+  int64_t cum = 0;
+  int cnt = 0;
 #pragma unroll 1
-    for (int it = 0; it < kExtractLimit && top != 0u; ++it) {
-      uint32_t c = 0u, nxt = 0u;
-#pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) {
-        const bool hit = rem[jj] == top;
-        c += hit ? 1u : 0u;
-        rem[jj] = hit ? 0u : rem[jj];
-        nxt = max(nxt, rem[jj]);
-      }
-      c = __reduce_add_sync(0xffffffffu, c);
-      const int64_t f = mass_fx_bits(top);
-      cum += (int64_t)c * f;
-      if (cum >= target) {
-        v = f;
-        found = true;
-        break;
-      }
-      top = __reduce_max_sync(0xffffffffu, nxt);
+  for (int it = 0; it < kExtractLimit && top != 0u; ++it) {
+    const bool hit = q[0] == top;
+    const uint32_t c = __reduce_add_sync(0xffffffffu, hit ? 1u : 0u);
+    const int64_t f = mass_fx_bits(top);
+    if (cum + (int64_t)c * f >= target) {
+      // v* = f; above 2^23 (masses >= 2^-29) the fixed point is exact, so
+      // the values greater than v* are exactly the ones taken so far
+      if (f >= (int64_t(1) << 23)) return eq6_word_from_cut<NJ>(fx, f, target, tol, lane, true, cum, cnt);
+      return eq6_word_from_cut<NJ>(fx, f, target, tol, lane);
     }
-    if (!found) {
-      uint32_t kk = 0u;
-      for (int bit = 31 - __clz(kmax_all); bit >= 0; --bit) {
-        const uint32_t cand = kk | (1u << bit);
-        int64_t sacc = 0;
+    cum += (int64_t)c * f;
+    cnt += (int)c;
+    if (hit) {
 #pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) sacc += (key[jj] >= cand) ? fx[jj] : 0;
-        if (warp_sum_u63(sacc) >= target) kk = cand;
-      }
-      v = mass_fx_bits(kk);
+      for (int jj = 0; jj + 1 < NJ; ++jj) q[jj] = q[jj + 1];
+      q[NJ - 1] = 0u;
     }
+    top = __reduce_max_sync(0xffffffffu, q[0]);
   }
-  return eq6_word_from_cut<NJ>(fx, v, target, tol, lane);
+  // bitwise search over the keys
+  uint32_t kk = 0u;
+  for (int bit = 31 - __clz(kmax_all); bit >= 0; --bit) {
+    const uint32_t cand = kk | (1u << bit);
+    int64_t sacc = 0;
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) sacc += (key[jj] >= cand) ? fx[jj] : 0;
+    if (warp_sum_u63(sacc) >= target) kk = cand;
+  }
+  return eq6_word_from_cut<NJ>(fx, mass_fx_bits(kk), target, tol, lane);
 }
 
 // The same step with a small footprint, for the discovery epilogue that

@@ -8,8 +8,9 @@ over the selected support, each step on its own seeded Q/K/V.
 The headline workload is the largest single-GPU configuration, the 32K
 context of the sweep (batch 1, 32 heads, head_dim 128, block 128). `value`
 is its late-step sparse attention throughput in useful TFLOP/s (4 d per
-admissible query-key pair inside the support), measured with CUDA events on
-the launching stream inside the timed trajectories. The line also carries ms
+admissible query-key pair inside the support), from the median of the late
+steps' CUDA-event times on the launching stream inside the timed
+trajectories. The line also carries ms
 per trajectory, the late-step time against the library's own dense kernel on
 the same inputs, the roofline of the dominant kernel, an end-to-end figure
 through the public API with host buffers, the fp64 CPU oracle timed on a
@@ -415,7 +416,7 @@ def run_gpu(args, rank, world):
     # host-to-device copies of a trajectory's step inputs run on rotating copy
     # streams, so that the copy of a later step overlaps the kernels of the
     # current one; each step's kernels wait for their own inputs only
-    copy_streams = [torch.cuda.Stream(dev) for _ in range(4)]
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(max(1, args.copy_streams))]
 
     def trajectory(inputs, record=False, out_host=None, host_inputs=None):
         launches = 0
@@ -523,11 +524,13 @@ def run_gpu(args, rank, world):
     h2d_gbs = h2d_bandwidth(dev)
 
     # ------------------------------------------------------------ aggregate over ranks
+    # the late step's time is the median of the timed launches (one host
+    # stall between an event and its launch would otherwise move a mean)
     sparse_ms, sparse_iqr = median_iqr(per["sparse"])
-    sparse_sum_ms = sum(per["sparse"]) / args.steps
-    traj_ms, sparse_sum_ms, e2e_traj_ms = reduce_max_over_ranks([traj_ms, sparse_sum_ms, e2e_traj_ms], world, dev)
+    sparse_mean_ms = sum(per["sparse"]) / len(per["sparse"])
+    traj_ms, sparse_ms, e2e_traj_ms = reduce_max_over_ranks([traj_ms, sparse_ms, e2e_traj_ms], world, dev)
     n_late = T - td
-    value = whole_job_tflops(n_late * sparse_flops, sparse_sum_ms, world)
+    value = whole_job_tflops(sparse_flops, sparse_ms, world)
     # e2e: the same late-step FLOPs over the whole host-to-host trajectory
     e2e_value = whole_job_tflops(n_late * sparse_flops, e2e_traj_ms, world)
 
@@ -580,6 +583,7 @@ def run_gpu(args, rank, world):
                    "l2": "each trajectory reads T distinct step inputs "
                          f"({T * 3 * B * H * n * d * 2 / 1e9:.2f} GB > 129 MB L2)"},
         "late_step_ms": round(sparse_ms, 4), "late_step_iqr_ms": round(sparse_iqr, 4),
+        "late_step_mean_ms": round(sparse_mean_ms, 4),
         "dense_step_ms": round(dense_ms, 4),
         "speedup_vs_dense": round(dense_ms / sparse_ms, 3),
         "dense_tflops": round(dense_tflops, 2), "frac_of_bf16_peak": round(value / world / peak_tf, 4),
@@ -836,6 +840,8 @@ def main():
                     help="comma-separated configurations of the per-configuration block, or 'none'")
     ap.add_argument("--passes", type=int, default=10, help="balanced passes per configuration")
     ap.add_argument("--reps", type=int, default=4, help="sparse and dense launches per pass")
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="streams the end-to-end run spreads its host-to-device copies over")
     ap.add_argument("--profile-kernel", default=None, choices=["discover", "discover_mass", "sparse", "select"],
                     help="only launch this kernel --steps times on --config (for ncu)")
     args = ap.parse_args()

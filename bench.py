@@ -187,7 +187,7 @@ class ClockSampler:
 def kernel_source_hash(kernel: str) -> str:
     """Hash of the sources a kernel is built from (the attention kernels, or
     the selection kernels)."""
-    names = (["select_kernel.cu", "select_step.cuh", "internal.h", "ptx.cuh"] if kernel == "select"
+    names = (["select_kernel.cu", "select_step.cuh", "select_keys.cuh", "internal.h", "ptx.cuh"] if kernel == "select"
              else ["attn_kernel.cuh", "ptx.cuh", "select_step.cuh", "internal.h"])
     h = hashlib.sha256()
     for name in names:

@@ -26,6 +26,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "select_keys.cuh"
 #include "select_step.cuh"
 
 namespace wise {
@@ -49,6 +50,7 @@ struct SelectParams {
   int32_t units_per_bh;
   int32_t qb_per_unit;  // query blocks per work unit (128 / block)
   int32_t group_heads;
+  int32_t order_segs;          // segments of a group's units, one warp and one counter table each
   int32_t mode;                // 0: Eq 6 with eta; 1: MassMatched; 2: SizeMatched
   const int32_t* ref_row_ptr;  // reference working set (modes 1 and 2)
   const int32_t* ref_col_idx;
@@ -70,29 +72,30 @@ __device__ __forceinline__ uint32_t step_eq6(const SelectParams& p, int bh, int 
     const int b = jj * 32 + lane;  // coalesced load order: jj-major
     m[jj] = (b < nadm) ? __ldg(src + b) : 0.f;
   }
-  int64_t fx[NJ];
   uint32_t key[NJ];
-  // every admissible mass of the row in [2^-29, 2^10) (the usual case): the
-  // fixed point is a plain shift; otherwise the general rounding
+#pragma unroll
+  for (int jj = 0; jj < NJ; ++jj) key[jj] = (jj * 32 + lane < nadm) ? mass_key(m[jj]) : 0u;
+  {
+    // the usual case: the cut among masses in [2^-29, 2^10), decided on the
+    // keys alone. A row of one round that needs more than 8 values (a flat
+    // row) takes the single pass over all 32 below instead.
+    uint32_t word;
+    if (eq6_step_word_keys<NJ, (NJ == 1 ? 8 : kExtractLimit)>(key, p.target_fx, p.tol_fx, lane, word)) return word;
+  }
+  int64_t fx[NJ];
+  // every admissible mass of the row in [2^-29, 2^10): the fixed point is a
+  // plain shift; otherwise the general rounding
   bool exact = true;
 #pragma unroll
   for (int jj = 0; jj < NJ; ++jj)
     exact &= (jj * 32 + lane >= nadm) || mass_fx_exact(__float_as_uint(m[jj]));
   if (__all_sync(0xffffffffu, exact)) {
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) {
-      const bool adm = jj * 32 + lane < nadm;
-      const uint32_t b = __float_as_uint(m[jj]);
-      fx[jj] = adm ? mass_fx_exact_bits(b) : INT64_MIN;
-      key[jj] = adm ? b : 0u;
-    }
+    for (int jj = 0; jj < NJ; ++jj)
+      fx[jj] = (jj * 32 + lane < nadm) ? mass_fx_exact_bits(__float_as_uint(m[jj])) : INT64_MIN;
   } else {
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) {
-      const bool adm = jj * 32 + lane < nadm;
-      fx[jj] = adm ? mass_fx(m[jj]) : INT64_MIN;
-      key[jj] = adm ? mass_key(m[jj]) : 0u;
-    }
+    for (int jj = 0; jj < NJ; ++jj) fx[jj] = (jj * 32 + lane < nadm) ? mass_fx(m[jj]) : INT64_MIN;
   }
   return eq6_step_word<NJ>(fx, key, p.target_fx, p.tol_fx, lane);
 }
@@ -111,24 +114,29 @@ __device__ __forceinline__ uint32_t step_eq6_any(const SelectParams& p, int bh, 
 }
 
 // Eq 6 over the window: one warp per (row, window step), window warps per
-// row, rows_per_cta rows per CTA. Each warp ORs its step support into the
-// row's words in shared memory; the row's step-0 warp then adds the sink /
+// row; a CTA takes one query block q of rows_per_cta (batch, head) slices.
+// blockIdx.y runs over q from the last query block down, so the CTAs with
+// the longest rows (q + 1 admissible blocks) start first and the short ones
+// fill the end of the launch. Each warp ORs its step support into the row's
+// words in shared memory; the row's step-0 warp then adds the sink /
 // diagonal blocks and writes the row's bitmask and count.
 template <int NJ>
 __global__ void __launch_bounds__(256, (NJ <= 8) ? 4 : 1) select_steps_kernel(const SelectParams p, int rows_per_cta) {
   __shared__ uint32_t rowbits[8][32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  // the finalize launch may be scheduled now; it waits for this grid to
+  // finish (and its writes to be visible) before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the finalize kernel that follows starts from a cleared look-back state
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < p.lb_words; i += blockDim.x) p.lb[i] = 0ull;
-  const int r_local = wid / p.window, w = wid % p.window;
-  const int64_t row = (int64_t)blockIdx.x * rows_per_cta + r_local;
-  const int64_t rows = (int64_t)p.bh_count * p.nb;
-  const bool live = r_local < rows_per_cta && row < rows;
+  const int r_local = wid / p.window, w = wid - r_local * p.window;
+  const int q = p.nb - 1 - (int)blockIdx.y;
+  const int bh = (int)blockIdx.x * rows_per_cta + r_local;
+  const bool live = r_local < rows_per_cta && bh < p.bh_count;
+  const int64_t row = (int64_t)bh * p.nb + q;
   if (w == 0 && r_local < rows_per_cta) rowbits[r_local][lane] = 0u;
   __syncthreads();
-  const int bh = live ? (int)(row / p.nb) : 0;
-  const int q = live ? (int)(row % p.nb) : 0;
   if (live) {
     const uint32_t word = step_eq6_any<NJ>(p, bh, q, w, lane);
     if (word) atomicOr(&rowbits[r_local][lane], word);
@@ -265,13 +273,13 @@ __global__ void __launch_bounds__(256) select_rows_kernel(const SelectParams p) 
 
 constexpr int kChunkRows = kSelectChunkRows;  // rows per finalize CTA (one per thread)
 constexpr int kOrderWarps = kChunkRows / 32;
+constexpr int kEmitStage = 1024;  // column entries staged per warp in the emit
 
 // Look-back state of the row_ptr scan: one word per chunk of kChunkRows
 // rows (flag in the top two bits: 1 = the chunk's own total, 2 = the total
-// of every row up to and including the chunk), then a ticket counter. It
-// sits after the bitmasks and counts in the workspace and is zeroed by the
-// selection kernel (or, for a finalize-only launch, by a memset) before the
-// finalize kernel runs.
+// of every row up to and including the chunk). It sits after the bitmasks
+// and counts in the workspace and is zeroed by the selection kernel (or, for
+// a finalize-only launch, by a memset) before the finalize kernel runs.
 constexpr uint64_t kLbAggregate = 1ull << 62, kLbInclusive = 2ull << 62, kLbValue = (1ull << 62) - 1;
 
 
@@ -286,53 +294,88 @@ __device__ __forceinline__ void st_release_gpu(uint64_t* p, uint64_t v) {
 
 // Rank the units of one group of (batch, head) slices by cost (listed
 // blocks), heaviest first, ties by unit index, and write their global order:
-// a stable counting sort. Warp w places the w-th eighth of the units, after
-// a per-warp histogram gives each warp its first position for every cost.
-// Shared memory: cost[units] | hist[kOrderWarps][maxc + 1] | start[maxc + 1],
+// a stable counting sort. The units are split into order_segs contiguous
+// segments (8, 16 or 32), each with its own counter table: the counts per
+// cost value of the segment's units, then the first position of the
+// segment's units of every cost. Warp w serves segments w, w + 8, ..., one
+// round of 32 units of each at a time, so the rounds of its segments
+// overlap instead of waiting on each other.
+// Shared memory: cost[units] | hist[order_segs][maxc + 1] | start[maxc + 1],
 // maxc = nb * qb_per_unit.
 __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
+  constexpr int kMaxSpw = 4;  // segments per warp
   const int h0 = g * p.group_heads;
   const int gsize = min(p.group_heads, p.bh_count - h0);
   const int units = gsize * p.units_per_bh;
   const int maxc = p.nb * p.qb_per_unit;
   const int nc = maxc + 1;
+  const int nseg = p.order_segs;
+  const int spw = nseg / kOrderWarps;
   int32_t* cost = sh;
   int32_t* hist = sh + units;
-  int32_t* start = hist + kOrderWarps * nc;
+  int32_t* start = hist + nseg * nc;
   __shared__ int32_t top_cost;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int c = tid; c < kOrderWarps * nc; c += blockDim.x) hist[c] = 0;
+  for (int c = tid; c < nseg * nc; c += blockDim.x) hist[c] = 0;
   if (tid == 0) top_cost = 0;
-  // costs: the listed blocks of the unit's query blocks (at most four); the
-  // counts of kBatch units per thread are all requested before any is used,
-  // so a thread's loads overlap instead of waiting on each other
+  // costs: the listed blocks of the unit's query blocks (at most four); each
+  // thread requests a batch of counts before it uses any, so its loads
+  // overlap instead of waiting on each other
   const int64_t row0 = (int64_t)h0 * p.nb;
   const int per_unit = p.qb_per_unit;
-  constexpr int kBatch = 16;
-  for (int base = 0; base < units; base += kBatch * (int)blockDim.x) {
-    int v[kBatch][4];
+  if (per_unit == 1) {
+    // one query block per unit: the group's rows in order
+    constexpr int kBatch = 32;
+    for (int base = 0; base < units; base += kBatch * (int)blockDim.x) {
+      int v[kBatch];
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int u = base + k * (int)blockDim.x + tid;
-      const int bh = u / p.units_per_bh, pr = u % p.units_per_bh;
-      const int nq = (u < units) ? min(per_unit, p.nb - pr * per_unit) : 0;
-      const int32_t* src = p.counts + row0 + (int64_t)bh * p.nb + pr * per_unit;
+      for (int k = 0; k < kBatch; ++k) {
+        const int u = base + k * (int)blockDim.x + tid;
+        v[k] = (u < units) ? __ldg(p.counts + row0 + u) : 0;
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[k][j] = (j < nq) ? __ldg(src + j) : 0;
+      for (int k = 0; k < kBatch; ++k) {
+        const int u = base + k * (int)blockDim.x + tid;
+        if (u < units) cost[u] = min(max(v[k], 0), maxc);
+      }
     }
+  } else {
+    constexpr int kBatch = 16;
+    for (int base = 0; base < units; base += kBatch * (int)blockDim.x) {
+      int v[kBatch][4];
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int u = base + k * (int)blockDim.x + tid;
-      if (u < units) cost[u] = min(max(v[k][0] + v[k][1] + v[k][2] + v[k][3], 0), maxc);
+      for (int k = 0; k < kBatch; ++k) {
+        const int u = base + k * (int)blockDim.x + tid;
+        const int bh = u / p.units_per_bh, pr = u % p.units_per_bh;
+        const int nq = (u < units) ? min(per_unit, p.nb - pr * per_unit) : 0;
+        const int32_t* src = p.counts + row0 + (int64_t)bh * p.nb + pr * per_unit;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[k][j] = (j < nq) ? __ldg(src + j) : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int u = base + k * (int)blockDim.x + tid;
+        if (u < units) cost[u] = min(max(v[k][0] + v[k][1] + v[k][2] + v[k][3], 0), maxc);
+      }
     }
   }
   __syncthreads();
-  const int seg = (units + kOrderWarps - 1) / kOrderWarps;
-  const int u_lo = min(units, warp * seg), u_hi = min(units, u_lo + seg);
+  const int seg = (units + nseg - 1) / nseg;
   int my_top = 0;
-  for (int u = u_lo + lane; u < u_hi; u += 32) {
-    atomicAdd(&hist[warp * nc + cost[u]], 1);
-    my_top = max(my_top, cost[u]);
+  for (int b = 0; b < seg; b += 32) {
+#pragma unroll
+    for (int k = 0; k < kMaxSpw; ++k) {
+      if (k < spw) {
+        const int sg = warp + kOrderWarps * k;
+        const int lo = min(units, sg * seg), hi = min(units, lo + seg);
+        const int u = lo + b + lane;
+        if (u < hi) {
+          const int c = cost[u];
+          atomicAdd(&hist[sg * nc + c], 1);
+          my_top = max(my_top, c);
+        }
+      }
+    }
   }
   my_top = __reduce_max_sync(0xffffffffu, (uint32_t)my_top);
   if (lane == 0) atomicMax(&top_cost, my_top);
@@ -341,8 +384,7 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
   // start[c] = number of units with a larger cost (exclusive scan from the top)
   for (int c = tid; c <= tc; c += blockDim.x) {
     int t = 0;
-#pragma unroll
-    for (int w = 0; w < kOrderWarps; ++w) t += hist[w * nc + c];
+    for (int w = 0; w < nseg; ++w) t += hist[w * nc + c];
     start[c] = t;
   }
   __syncthreads();
@@ -362,63 +404,93 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
     }
   }
   __syncthreads();
-  // first position of warp w's units of cost c
+  // first position of segment w's units of cost c
   for (int c = tid; c <= tc; c += blockDim.x) {
     int run = start[c];
-#pragma unroll
-    for (int w = 0; w < kOrderWarps; ++w) {
+    for (int w = 0; w < nseg; ++w) {
       const int h = hist[w * nc + c];
       hist[w * nc + c] = run;
       run += h;
     }
   }
   __syncthreads();
-  // place the warp's units in index order, 32 at a time; equal costs keep index order
+  // place each segment's units in index order, 32 at a time; equal costs
+  // keep index order. The reads of all of the warp's segments come before
+  // any of their writes (each segment has its own table).
   const int64_t gbase = (int64_t)h0 * p.units_per_bh;
-  int32_t* base_w = hist + warp * nc;
-  for (int b = u_lo; b < u_hi; b += 32) {
-    const int u = b + lane;
-    const bool in = u < u_hi;
-    const int c = in ? cost[u] : -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, c);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const int base = in ? base_w[c] : 0;
+  for (int b = 0; b < seg; b += 32) {
+    int cs[kMaxSpw], us[kMaxSpw], bases[kMaxSpw];
+    uint32_t peers[kMaxSpw];
+#pragma unroll
+    for (int k = 0; k < kMaxSpw; ++k) {
+      const int sg = warp + kOrderWarps * k;
+      const int lo = min(units, sg * seg), hi = min(units, lo + seg);
+      us[k] = lo + b + lane;
+      cs[k] = (k < spw && us[k] < hi) ? cost[us[k]] : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxSpw; ++k) peers[k] = (k < spw) ? __match_any_sync(0xffffffffu, cs[k]) : 0u;
+#pragma unroll
+    for (int k = 0; k < kMaxSpw; ++k)
+      bases[k] = (cs[k] >= 0) ? hist[(warp + kOrderWarps * k) * nc + cs[k]] : 0;
     __syncwarp();
-    if (in) {
-      p.tile_order[gbase + base + rank] = (int32_t)(gbase + u);
-      if (rank == 0) base_w[c] = base + __popc(peers);
+#pragma unroll
+    for (int k = 0; k < kMaxSpw; ++k) {
+      if (cs[k] >= 0) {
+        const int rank = __popc(peers[k] & ((1u << lane) - 1u));
+        p.tile_order[gbase + bases[k] + rank] = (int32_t)(gbase + us[k]);
+        if (rank == 0) hist[(warp + kOrderWarps * k) * nc + cs[k]] = bases[k] + __popc(peers[k]);
+      }
     }
     __syncwarp();
   }
 }
 
-// Finalize, one launch: the first n_chunks CTAs to start take chunks of
-// kChunkRows rows in the order of their tickets, get the count of all earlier
-// rows from the chunks before them (decoupled look-back: a chunk publishes its
-// own total at once and the running total as soon as it knows it), write
-// their row_ptr entries and emit their rows' column lists in ascending order;
-// the remaining CTAs build the late-step work order, one group each.
+// Finalize, one launch: CTA k < n_chunks takes the k-th chunk of kChunkRows
+// rows, gets the count of all earlier rows from the chunks before it
+// (decoupled look-back: a chunk publishes its own total at once and the
+// running total as soon as it knows it), writes its row_ptr entries and
+// emits its rows' column lists in ascending order; the remaining CTAs build
+// the late-step work order, one group each. CTAs are dispatched in index
+// order, so every chunk a CTA waits for is already running (the usual
+// assumption of a single-pass scan); the wait is bounded all the same.
 __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectParams p, int n_chunks, uint64_t* lb) {
   extern __shared__ int32_t sh[];
   __shared__ int32_t red[kOrderWarps];
   __shared__ int32_t start_s[kChunkRows];
   __shared__ int32_t cnt_s[kChunkRows];
-  __shared__ uint32_t s_ticket;
   __shared__ int64_t s_prefix;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // launched early after the Eq 6 kernel: wait until its bitmasks, counts
+  // and cleared look-back state are complete and visible (a no-op after an
+  // ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if ((int)blockIdx.x >= n_chunks) {
     order_group(p, blockIdx.x - n_chunks, sh);
     return;
   }
   uint64_t* state = lb;
-  unsigned int* ticket = reinterpret_cast<unsigned int*>(lb + n_chunks);
-  if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
-  __syncthreads();
-  const int chunk = (int)s_ticket;
   const int64_t rows = (int64_t)p.bh_count * p.nb;
+  const int chunk = (int)blockIdx.x;
   const int64_t r0 = (int64_t)chunk * kChunkRows;
+  const int nrows = (int)min((int64_t)kChunkRows, rows - r0);
   const int64_t r = r0 + tid;
-  const int c = (r < rows) ? __ldg(p.counts + r) : 0;
+  const int c = (tid < nrows) ? __ldg(p.counts + r) : 0;
+  // the chunk's bit words, read coalesced into shared memory (row stride
+  // nwords + 1, so that the lanes of a warp reading consecutive rows' words
+  // hit distinct banks); behind them, the warps' staging areas for the emit
+  const int nw = p.nwords, stride = nw + 1;
+  uint32_t* bits_s = reinterpret_cast<uint32_t*>(sh);
+  uint32_t* stage = bits_s + kChunkRows * stride;
+  {
+    const uint32_t* src = p.bits + r0 * nw;
+    const int total = nrows * nw;
+#pragma unroll 4
+    for (int i = tid; i < total; i += kChunkRows) {
+      const int rr = i / nw;
+      bits_s[rr * stride + (i - rr * nw)] = __ldg(src + i);
+    }
+  }
   cnt_s[tid] = c;
   // exclusive scan of this chunk's counts
   int inc = c;
@@ -477,26 +549,45 @@ __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectPar
     if (start + c > p.col_cap) atomicOr(p.err, kErrBadSupport);
   }
   __syncthreads();
-  // emit, one lane per row: lane l of warp w writes row w + 8 l, its set
-  // bits in ascending order from the row's start (rows past the end hold no
-  // bits; a row over capacity is flagged above)
+  // emit: warp w writes the column lists of rows 32 w .. 32 w + 31, which
+  // are contiguous in col_idx. Each lane expands its row's set bits, in
+  // ascending order, into the warp's staging area; the warp then copies the
+  // area out with consecutive lanes on consecutive entries. A warp whose
+  // lists exceed the area or the capacity writes each row directly instead
+  // (a row over capacity is flagged above and skipped). A lane writes at
+  // most its row's count.
   {
-    const int i = warp + kOrderWarps * lane;
-    const int64_t row = r0 + i;
-    if (row < rows) {
-      int64_t pos = start_s[i];
-      const int64_t end = pos + cnt_s[i];
-      if (end <= p.col_cap) {
-        const uint32_t* wp = p.bits + row * p.nwords;
-        for (int w0 = 0; w0 < p.nwords; w0 += 8) {
-          uint32_t rw[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) rw[j] = (w0 + j < p.nwords) ? __ldg(wp + w0 + j) : 0u;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t x = rw[j];
+    const int i = 32 * warp + lane;
+    const bool have = i < nrows;
+    const int64_t my_start = have ? start_s[i] : 0;
+    const int my_cnt = have ? cnt_s[i] : 0;
+    const int64_t ws = __shfl_sync(0xffffffffu, my_start, 0);
+    const int wn = warp_sum32(my_cnt);
+    if (32 * warp < nrows) {
+      const uint32_t* rowbits = bits_s + i * stride;
+      if (ws + wn <= p.col_cap && wn <= kEmitStage) {
+        uint32_t* st = stage + warp * kEmitStage;
+        if (have) {
+          int off = (int)(my_start - ws);
+          const int lim = off + my_cnt;
+          for (int j = 0; j < nw; ++j) {
+            uint32_t x = rowbits[j];
+            while (x && off < lim) {
+              st[off++] = 32u * j + __ffs(x) - 1;
+              x &= x - 1;
+            }
+          }
+        }
+        __syncwarp();
+        for (int e = lane; e < wn; e += 32) p.col_idx[ws + e] = (int32_t)st[e];
+      } else if (have) {
+        int64_t pos = my_start;
+        const int64_t end = pos + my_cnt;
+        if (end <= p.col_cap) {
+          for (int j = 0; j < nw; ++j) {
+            uint32_t x = rowbits[j];
             while (x && pos < end) {
-              p.col_idx[pos++] = 32 * (w0 + j) + __ffs(x) - 1;
+              p.col_idx[pos++] = 32 * j + __ffs(x) - 1;
               x &= x - 1;
             }
           }
@@ -526,14 +617,20 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   p.units_per_bh = s.units_per_bh;
   p.qb_per_unit = s.qb_per_unit;
   // ranking groups: all slices in one group when its counting sort fits in
-  // shared memory (cost per unit + per-warp and total counters per cost value)
+  // shared memory (cost per unit + per-segment and total counters per cost
+  // value); 32 segments when their counters take at most half of it, else
+  // 16 or 8
   {
     constexpr size_t kOrderSmem = 200u * 1024u;
-    const size_t fixed = ((size_t)s.nb * s.qb_per_unit + 1) * sizeof(int32_t) * (kOrderWarps + 1);
+    const size_t nc = (size_t)s.nb * s.qb_per_unit + 1;
+    int segs = 4 * kOrderWarps;
+    while (segs > kOrderWarps && nc * sizeof(int32_t) * (segs + 1) > kOrderSmem / 2) segs >>= 1;
+    const size_t fixed = nc * sizeof(int32_t) * (segs + 1);
     const size_t per_slice = (size_t)s.units_per_bh * sizeof(int32_t);
     int64_t g = s.bh_count;
     if (fixed + per_slice * (size_t)g > kOrderSmem) g = (int64_t)((kOrderSmem - fixed) / per_slice);
     p.group_heads = (int32_t)(g < 1 ? 1 : g);
+    p.order_segs = segs;
   }
   p.mode = s.mode;
   p.ref_row_ptr = s.ref_row_ptr;
@@ -547,7 +644,7 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   const int rounds = (s.nb + 31) / 32;
   // Eq 6: window warps per row, as many rows per CTA as fit in 8 warps
   const int rpc = (s.window >= 1 && s.window <= 8) ? 8 / s.window : 1;
-  const unsigned grid_steps = (unsigned)((rows + rpc - 1) / rpc);
+  const dim3 grid_steps((unsigned)((s.bh_count + rpc - 1) / rpc), (unsigned)s.nb);
   const unsigned threads_steps = (unsigned)(32 * s.window * rpc);
   if (s.finalize_only) {
     // the row bitmasks and counts come from the discovery epilogue
@@ -568,15 +665,30 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
   else select_rows_kernel<32><<<grid_rows, 256, 0, stream>>>(p);
   const int n_chunks = (int)((rows + kChunkRows - 1) / kChunkRows);
   const int groups = s.tile_order ? (s.bh_count + p.group_heads - 1) / p.group_heads : 0;
-  const size_t shm = s.tile_order ? ((size_t)p.group_heads * s.units_per_bh +
-                                     (size_t)(kOrderWarps + 1) * ((size_t)s.nb * s.qb_per_unit + 1)) *
-                                        sizeof(int32_t)
-                                  : 0;
+  const size_t shm_order = s.tile_order ? ((size_t)p.group_heads * s.units_per_bh +
+                                           (size_t)(p.order_segs + 1) * ((size_t)s.nb * s.qb_per_unit + 1)) *
+                                              sizeof(int32_t)
+                                        : 0;
+  const size_t shm_chunk = ((size_t)kChunkRows * (p.nwords + 1) + (size_t)kOrderWarps * kEmitStage) * sizeof(uint32_t);
+  const size_t shm = shm_order > shm_chunk ? shm_order : shm_chunk;
   if (shm > 40 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
     if (e != cudaSuccess) return e;
   }
-  finalize_kernel<<<n_chunks + groups, kChunkRows, shm, stream>>>(p, n_chunks, p.lb);
+  // after the Eq 6 kernel, finalize is a programmatic dependent launch: its
+  // CTAs are scheduled while the last Eq 6 CTAs run
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n_chunks + groups));
+  cfg.blockDim = dim3(kChunkRows);
+  cfg.dynamicSmemBytes = shm;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = (!s.finalize_only && s.mode == 0) ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, finalize_kernel, p, n_chunks, p.lb);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -153,8 +153,14 @@ def _check_tile_order(sup):
     # first, ties by unit index.
     qpu = 128 // sup.block
     nb = sup.seq_len // sup.block
-    # the ranking CTA holds one cost per unit and nine counters per cost value
-    if (units + 9 * (nb * qpu + 1)) * 4 <= 200 * 1024:
+    # the ranking CTA holds one cost per unit and, per cost value, a counter
+    # for each of its segments (32, or fewer when 33 counters per value take
+    # more than 100 KB, down to 8) plus a total
+    nc = nb * qpu + 1
+    segs = 32
+    while segs > 8 and nc * 4 * (segs + 1) > 100 * 1024:
+        segs //= 2
+    if (units + (segs + 1) * nc) * 4 <= 200 * 1024:
         counts = np.diff(sup.row_ptr.cpu().numpy().astype(np.int64)).reshape(sup.batch * sup.heads, nb)
         tiles = units // (sup.batch * sup.heads)
         pad = np.zeros((sup.batch * sup.heads, tiles * qpu), np.int64)
@@ -192,6 +198,52 @@ def test_select_bit_exact_where_the_fixed_point_rounds(nb, lo_exp, hi_exp, eta):
     sup = wise.select_support(torch.from_numpy(m).cuda(), nb * 64, 64, 64, eta, 0)
     wise.check_device()
     rp_ref, ci_ref = O.select(m.astype(np.float64), eta, 0)
+    rp = sup.row_ptr.cpu().numpy()
+    assert np.array_equal(rp, rp_ref)
+    assert np.array_equal(sup.col_idx.cpu().numpy()[:rp[-1]], ci_ref)
+
+
+def _structured_mass_rows(nb, seed):
+    """Rows whose Eq 6 cut falls in large groups of equal or near-equal
+    masses, or near the smallest masses the selection kernel decides on the
+    masses' float keys alone (a cut v* within the 1e-6 tie tolerance of
+    2^-29): uniform rows (every admissible block equal), rows whose 40
+    heaviest blocks lie within 8e-7 of each other, rows with one block at 0.5
+    and the rest near 2^-20 or 2^-19, and rows with a mass above 1."""
+    rng = np.random.default_rng(seed)
+    m = np.zeros((2, 1, 1, nb, nb), np.float32)
+    for w in range(2):
+        for q in range(nb):
+            kind = (q + w) % 5
+            n = q + 1
+            if kind == 0:
+                r = np.full(n, 1.0 / n)
+            elif kind == 1:
+                r = rng.dirichlet(np.full(n, 0.3)) * 0.05
+                top = rng.choice(n, size=min(n, 40), replace=False)
+                r[top] = 0.95 / len(top) + rng.uniform(-4e-7, 4e-7, len(top))
+            elif kind == 2:
+                r = 2.0 ** -20 * (1 + rng.uniform(0, 2 ** -10, n))
+                r[0] = 0.5
+            elif kind == 3:
+                r = 2.0 ** -19 * (1 + rng.uniform(0, 0.5, n))
+                r[0] = 0.5
+            else:
+                r = rng.dirichlet(np.full(n, 0.5))
+                r[rng.integers(n)] = 3.0
+            m[w, 0, 0, q, :n] = r.astype(np.float32)
+    return m
+
+
+@pytest.mark.parametrize("nb,eta", [(64, 0.9), (300, 0.9), (300, 0.5 + 2.0 ** -12), (1024, 0.95)])
+def test_select_bit_exact_on_tie_groups_and_cut_boundaries(nb, eta):
+    """Cuts inside large exact- and near-tie groups (where the near group is
+    only partly taken, lowest index first) and cuts at the edge of the range
+    the kernel decides on float keys: the CSR must equal the oracle's."""
+    m = _structured_mass_rows(nb, seed=nb)
+    sup = wise.select_support(torch.from_numpy(m).cuda(), nb * 64, 64, 64, eta, 3)
+    wise.check_device()
+    rp_ref, ci_ref = O.select(m.astype(np.float64), eta, 3)
     rp = sup.row_ptr.cpu().numpy()
     assert np.array_equal(rp, rp_ref)
     assert np.array_equal(sup.col_idx.cpu().numpy()[:rp[-1]], ci_ref)

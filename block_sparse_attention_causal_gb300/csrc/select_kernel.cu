@@ -51,6 +51,7 @@ struct SelectParams {
   int32_t qb_per_unit;  // query blocks per work unit (128 / block)
   int32_t group_heads;
   int32_t order_segs;          // segments of a group's units, one warp and one counter table each
+  int32_t direct_rows;         // chunks starting at most this many rows in sum the earlier counts directly
   int32_t mode;                // 0: Eq 6 with eta; 1: MassMatched; 2: SizeMatched
   const int32_t* ref_row_ptr;  // reference working set (modes 1 and 2)
   const int32_t* ref_col_idx;
@@ -312,11 +313,8 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
   const int nseg = p.order_segs;
   const int spw = nseg / kOrderWarps;
   int32_t* cost = sh;
-  int32_t* hist = sh + units;
-  int32_t* start = hist + nseg * nc;
   __shared__ int32_t top_cost;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int c = tid; c < nseg * nc; c += blockDim.x) hist[c] = 0;
   if (tid == 0) top_cost = 0;
   // costs: the listed blocks of the unit's query blocks (at most four); each
   // thread requests a batch of counts before it uses any, so its loads
@@ -324,19 +322,48 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
   const int64_t row0 = (int64_t)h0 * p.nb;
   const int per_unit = p.qb_per_unit;
   if (per_unit == 1) {
-    // one query block per unit: the group's rows in order
-    constexpr int kBatch = 32;
-    for (int base = 0; base < units; base += kBatch * (int)blockDim.x) {
-      int v[kBatch];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int u = base + k * (int)blockDim.x + tid;
-        v[k] = (u < units) ? __ldg(p.counts + row0 + u) : 0;
+    // one query block per unit: the group's rows in order, raw (clamped
+    // where they are read). Taken by the TMA unit in bulk when aligned: a
+    // single SM's own loads of this many counts wait on its few outstanding
+    // misses.
+    const int32_t* src = p.counts + row0;
+    const uint32_t bytes = (uint32_t)units * 4u;
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(cost)) & 15u) == 0 && (bytes & 15u) == 0) {
+      if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
       }
+      __syncthreads();
+      if (tid == 0) {
+        constexpr uint32_t kPiece = 16384;
+        mbar_arrive_expect_tx(&bar, bytes);
+        for (uint32_t off = 0; off < bytes; off += kPiece) {
+          const uint32_t n = min(kPiece, bytes - off);
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  smem_u32(reinterpret_cast<uint8_t*>(cost) + off)),
+              "l"(reinterpret_cast<const uint8_t*>(src) + off), "r"(n), "r"(smem_u32(&bar))
+              : "memory");
+        }
+      }
+      mbar_wait<7>(&bar, 0, &abort_flag, p.err);
+    } else {
+      constexpr int kBatch = 32;
+      for (int base = 0; base < units; base += kBatch * (int)blockDim.x) {
+        int v[kBatch];
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int u = base + k * (int)blockDim.x + tid;
-        if (u < units) cost[u] = min(max(v[k], 0), maxc);
+        for (int k = 0; k < kBatch; ++k) {
+          const int u = base + k * (int)blockDim.x + tid;
+          v[k] = (u < units) ? __ldg(src + u) : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int u = base + k * (int)blockDim.x + tid;
+          if (u < units) cost[u] = v[k];
+        }
       }
     }
   } else {
@@ -360,6 +387,11 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
     }
   }
   __syncthreads();
+  const int64_t gbase = (int64_t)h0 * p.units_per_bh;
+  int32_t* hist = cost + units;
+  int32_t* start = hist + nseg * nc;
+  for (int c = tid; c < nseg * nc; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
   const int seg = (units + nseg - 1) / nseg;
   int my_top = 0;
   for (int b = 0; b < seg; b += 32) {
@@ -370,14 +402,14 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
         const int lo = min(units, sg * seg), hi = min(units, lo + seg);
         const int u = lo + b + lane;
         if (u < hi) {
-          const int c = cost[u];
+          const int c = min(max(cost[u], 0), maxc);
           atomicAdd(&hist[sg * nc + c], 1);
           my_top = max(my_top, c);
         }
       }
     }
   }
-  my_top = __reduce_max_sync(0xffffffffu, (uint32_t)my_top);
+  my_top = (int)__reduce_max_sync(0xffffffffu, (uint32_t)my_top);
   if (lane == 0) atomicMax(&top_cost, my_top);
   __syncthreads();
   const int tc = top_cost;
@@ -417,7 +449,6 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
   // place each segment's units in index order, 32 at a time; equal costs
   // keep index order. The reads of all of the warp's segments come before
   // any of their writes (each segment has its own table).
-  const int64_t gbase = (int64_t)h0 * p.units_per_bh;
   for (int b = 0; b < seg; b += 32) {
     int cs[kMaxSpw], us[kMaxSpw], bases[kMaxSpw];
     uint32_t peers[kMaxSpw];
@@ -426,7 +457,7 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
       const int sg = warp + kOrderWarps * k;
       const int lo = min(units, sg * seg), hi = min(units, lo + seg);
       us[k] = lo + b + lane;
-      cs[k] = (k < spw && us[k] < hi) ? cost[us[k]] : -1;
+      cs[k] = (k < spw && us[k] < hi) ? min(max(cost[us[k]], 0), maxc) : -1;
     }
 #pragma unroll
     for (int k = 0; k < kMaxSpw; ++k) peers[k] = (k < spw) ? __match_any_sync(0xffffffffu, cs[k]) : 0u;
@@ -455,11 +486,14 @@ __device__ void order_group(const SelectParams& p, int g, int32_t* sh) {
 // order, so every chunk a CTA waits for is already running (the usual
 // assumption of a single-pass scan); the wait is bounded all the same.
 __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectParams p, int n_chunks, uint64_t* lb) {
-  extern __shared__ int32_t sh[];
+  extern __shared__ __align__(16) int32_t sh[];
   __shared__ int32_t red[kOrderWarps];
   __shared__ int32_t start_s[kChunkRows];
   __shared__ int32_t cnt_s[kChunkRows];
   __shared__ int64_t s_prefix;
+  __shared__ int64_t red64[kOrderWarps];
+  __shared__ uint64_t pre_bar;
+  __shared__ int pre_abort;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // launched early after the Eq 6 kernel: wait until its bitmasks, counts
   // and cleared look-back state are complete and visible (a no-op after an
@@ -491,6 +525,28 @@ __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectPar
       bits_s[rr * stride + (i - rr * nw)] = __ldg(src + i);
     }
   }
+  // A chunk that starts within the first direct_rows rows sums the counts of
+  // all earlier rows itself (one bulk copy into shared memory) instead of
+  // waiting for the chunks before it; the others look back.
+  int32_t* pre_s = reinterpret_cast<int32_t*>(stage + kOrderWarps * kEmitStage);
+  const bool direct = chunk > 0 && r0 <= (int64_t)p.direct_rows &&
+                      (reinterpret_cast<uintptr_t>(p.counts) & 15u) == 0;
+  if (direct && tid == 0) {
+    pre_abort = 0;
+    mbar_init(&pre_bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = (uint32_t)r0 * 4u;
+    constexpr uint32_t kPiece = 16384;
+    mbar_arrive_expect_tx(&pre_bar, bytes);
+    for (uint32_t off = 0; off < bytes; off += kPiece) {
+      const uint32_t n = min(kPiece, bytes - off);
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_u32(reinterpret_cast<uint8_t*>(pre_s) + off)),
+          "l"(reinterpret_cast<const uint8_t*>(p.counts) + off), "r"(n), "r"(smem_u32(&pre_bar))
+          : "memory");
+    }
+  }
   cnt_s[tid] = c;
   // exclusive scan of this chunk's counts
   int inc = c;
@@ -507,7 +563,21 @@ __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectPar
     wpre += (w < warp) ? red[w] : 0;
     total += red[w];
   }
-  if (warp == 0) {
+  if (direct) {
+    mbar_wait<8>(&pre_bar, 0, &pre_abort, p.err);
+    int part = 0;
+    for (int i = tid; i < (int)r0; i += kChunkRows) part += pre_s[i];
+    part = warp_sum32(part);
+    if (lane == 0) red64[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+      int64_t prefix = 0;
+#pragma unroll
+      for (int w = 0; w < kOrderWarps; ++w) prefix += red64[w];
+      st_release_gpu(state + chunk, kLbInclusive | (uint64_t)(prefix + total));
+      s_prefix = prefix;
+    }
+  } else if (warp == 0) {
     // look back over the chunks before this one, 32 at a time
     if (lane == 0)
       st_release_gpu(state + chunk, (chunk == 0 ? kLbInclusive : kLbAggregate) | (uint64_t)total);
@@ -598,7 +668,7 @@ __global__ void __launch_bounds__(kChunkRows, 1) finalize_kernel(const SelectPar
 }
 
 cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
-  SelectParams p;
+  SelectParams p = {};
   p.mass = s.mass;
   p.window = s.window;
   p.bh_count = s.bh_count;
@@ -669,7 +739,12 @@ cudaError_t launch_select(const SelectLaunch& s, cudaStream_t stream) {
                                            (size_t)(p.order_segs + 1) * ((size_t)s.nb * s.qb_per_unit + 1)) *
                                               sizeof(int32_t)
                                         : 0;
-  const size_t shm_chunk = ((size_t)kChunkRows * (p.nwords + 1) + (size_t)kOrderWarps * kEmitStage) * sizeof(uint32_t);
+  // chunks within the first kDirectRows rows sum the earlier counts directly
+  constexpr int64_t kDirectRows = 16384;
+  p.direct_rows = (int32_t)(rows < kDirectRows ? rows : kDirectRows);
+  const size_t shm_chunk =
+      ((size_t)kChunkRows * (p.nwords + 1) + (size_t)kOrderWarps * kEmitStage + (size_t)p.direct_rows) *
+      sizeof(uint32_t);
   const size_t shm = shm_order > shm_chunk ? shm_order : shm_chunk;
   if (shm > 40 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);

@@ -188,7 +188,7 @@ def kernel_source_hash(kernel: str) -> str:
     """Hash of the sources a kernel is built from (the attention kernels, or
     the selection kernels)."""
     names = (["select_kernel.cu", "select_step.cuh", "select_keys.cuh", "internal.h", "ptx.cuh"] if kernel == "select"
-             else ["attn_kernel.cuh", "ptx.cuh", "select_step.cuh", "internal.h"])
+             else ["attn_kernel.cuh", "ptx.cuh", "select_step.cuh", "gather.cuh", "internal.h"])
     h = hashlib.sha256()
     for name in names:
         with open(os.path.join(ROOT, "block_sparse_attention_causal_gb300", "csrc", name), "rb") as f:

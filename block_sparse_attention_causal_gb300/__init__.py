@@ -32,7 +32,7 @@ from ._lib import (WISE_BF16, WISE_F32, WISE_SUPPORT_DIAG, WISE_SUPPORT_SINK, Wi
 __all__ = ["discover", "select_support", "sparse", "Support", "device_status", "WiseError", "discover_select",
            "select_finalize", "new_select_state",
            "WISE_SUPPORT_SINK", "WISE_SUPPORT_DIAG", "useful_flops", "dense_flops", "retained_mass",
-           "support_jaccard", "select_control"]
+           "support_jaccard", "select_control", "gather_plan"]
 
 _OUT = {torch.bfloat16: WISE_BF16, torch.float32: WISE_F32}
 
@@ -243,6 +243,9 @@ class Support:
     seq_len: int
     head_dim: int
     block: int
+    # blocks of 32: the late steps' gathered entries of every tile, built once
+    # from the CSR by gather_plan (None: each late step forms them itself)
+    plan: Optional[torch.Tensor] = None
 
     @property
     def n_blocks(self) -> int:
@@ -257,8 +260,10 @@ class Support:
 def select_support(masses: torch.Tensor, seq_len: int, head_dim: int, block: int, eta: float,
                    flags: int = WISE_SUPPORT_SINK | WISE_SUPPORT_DIAG, *,
                    support: Optional[Support] = None, workspace: Optional[torch.Tensor] = None,
-                   stream: Optional[torch.cuda.Stream] = None) -> Support:
-    """Working-set selection from the window's masses [W, B, H, nb, nb] (f32)."""
+                   plan: bool = True, stream: Optional[torch.cuda.Stream] = None) -> Support:
+    """Working-set selection from the window's masses [W, B, H, nb, nb] (f32).
+    With blocks of 32 (and plan), the late steps' gathered entries are built
+    too (gather_plan)."""
     if not masses.is_cuda or masses.dtype != torch.float32 or masses.dim() != 5 or not masses.is_contiguous():
         raise ValueError("masses must be a contiguous float32 CUDA tensor [W, B, H, nb, nb]")
     _check_device("masses", masses)
@@ -287,15 +292,40 @@ def select_support(masses: torch.Tensor, seq_len: int, head_dim: int, block: int
                                  support.tile_order.data_ptr(), support.nnz.data_ptr(), workspace.data_ptr(),
                                  workspace.numel(), _stream_handle(stream))
     _lib.check(st, "wise_select_support")
+    if block == 32 and plan:
+        gather_plan(support, stream=stream)
+    return support
+
+
+def gather_plan(support: Support, *, stream: Optional[torch.cuda.Stream] = None) -> Support:
+    """For blocks of 32: build (or rebuild) support.plan, the late steps'
+    gathered entries of every 128-row tile, from the support's CSR. Call it
+    again whenever the CSR changes. Other block sizes have no plan."""
+    if support.block != 32:
+        support.plan = None
+        return support
+    lib = _lib.load()
+    desc = _lib.make_desc(support.batch, support.heads, support.seq_len, support.head_dim, support.block)
+    dev = support.row_ptr.device
+    _check_support("support", support, dev, int(lib.wise_schedule_units(desc)))
+    nbytes = int(lib.wise_gather_plan_bytes(desc))
+    if support.plan is None or support.plan.numel() < nbytes or support.plan.device != dev:
+        support.plan = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _check_bytes("plan", support.plan, nbytes, dev)
+    st = lib.wise_gather_plan(desc, support.row_ptr.data_ptr(), support.col_idx.data_ptr(), support.col_idx.numel(),
+                              support.plan.data_ptr(), support.plan.numel(), _stream_handle(stream))
+    _lib.check(st, "wise_gather_plan")
     return support
 
 
 def sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, support: Support, *, want_lse: bool = True,
            out_dtype: torch.dtype = torch.bfloat16, scale: float = 0.0, out: Optional[torch.Tensor] = None,
-           lse: Optional[torch.Tensor] = None, use_schedule: bool = True,
+           lse: Optional[torch.Tensor] = None, use_schedule: bool = True, use_plan: bool = True,
            stream: Optional[torch.cuda.Stream] = None):
     """Late (reuse) step over the support. Returns (O, LSE or None).
-    k and v may have fewer heads than q (grouped-query attention)."""
+    k and v may have fewer heads than q (grouped-query attention). With
+    blocks of 32 and a support.plan (use_plan), the tiles' gathered entries
+    are read from the plan; the results are the same bits either way."""
     hk = _check_qkv(q, k, v)
     lib = _lib.load()
     b, h, n, d = q.shape
@@ -311,12 +341,19 @@ def sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, support: Support, 
         lse = torch.empty((b, h, n), dtype=torch.float32, device=dev)
     if want_lse:
         _check_buffer("lse", lse, torch.float32, (b, h, n), dev)
-    st = lib.wise_attn_sparse(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), support.row_ptr.data_ptr(),
-                              support.col_idx.data_ptr(), support.col_idx.numel(),
-                              support.tile_order.data_ptr() if (use_schedule and support.tile_order is not None)
-                              else None, out.data_ptr(),
-                              _ptr(lse) if want_lse else None, _stream_handle(stream))
-    _lib.check(st, "wise_attn_sparse")
+    order = support.tile_order.data_ptr() if (use_schedule and support.tile_order is not None) else None
+    if use_plan and support.plan is not None and support.block == 32:
+        _check_bytes("support.plan", support.plan, int(lib.wise_gather_plan_bytes(desc)), dev)
+        st = lib.wise_attn_sparse_planned(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), support.row_ptr.data_ptr(),
+                                          support.col_idx.data_ptr(), support.col_idx.numel(), order,
+                                          support.plan.data_ptr(), out.data_ptr(), _ptr(lse) if want_lse else None,
+                                          _stream_handle(stream))
+        _lib.check(st, "wise_attn_sparse_planned")
+    else:
+        st = lib.wise_attn_sparse(desc, q.data_ptr(), k.data_ptr(), v.data_ptr(), support.row_ptr.data_ptr(),
+                                  support.col_idx.data_ptr(), support.col_idx.numel(), order, out.data_ptr(),
+                                  _ptr(lse) if want_lse else None, _stream_handle(stream))
+        _lib.check(st, "wise_attn_sparse")
     return out, (lse if want_lse else None)
 
 
@@ -347,6 +384,8 @@ def select_finalize(select_state: torch.Tensor, batch: int, heads: int, seq_len:
                                   support.col_idx.data_ptr(), support.col_idx.numel(),
                                   support.tile_order.data_ptr(), support.nnz.data_ptr(), _stream_handle(stream))
     _lib.check(st, "wise_select_finalize")
+    if block == 32:
+        gather_plan(support, stream=stream)
     return support
 
 

@@ -34,7 +34,8 @@ EXPORTS = (
     "wise_schedule_units", "wise_support_capacity", "wise_select_workspace", "wise_select_support",
     "wise_attn_sparse", "wise_validate_support", "wise_device_status", "wise_select_support_noalloc",
     "wise_support_retained_mass", "wise_support_jaccard", "wise_select_control", "wise_attn_discover_select",
-    "wise_select_finalize", "wise_validate_schedule", "wise_wait_expiry_check",
+    "wise_select_finalize", "wise_validate_schedule", "wise_wait_expiry_check", "wise_gather_plan_bytes",
+    "wise_gather_plan", "wise_attn_sparse_planned",
 )
 
 
@@ -89,6 +90,9 @@ _SIGNATURES = {
                                                  _i32, _i32, _vp, _sz, _vp]),
     "wise_select_finalize": (ctypes.c_int, [_dp, _vp, _sz, _vp, _vp, _i64, _vp, _vp, _vp]),
     "wise_validate_schedule": (ctypes.c_int, [_dp, _vp]),
+    "wise_gather_plan_bytes": (ctypes.c_size_t, [_dp]),
+    "wise_gather_plan": (ctypes.c_int, [_dp, _vp, _vp, _i64, _vp, ctypes.c_size_t, _vp]),
+    "wise_attn_sparse_planned": (ctypes.c_int, [_dp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp]),
     "wise_wait_expiry_check": (ctypes.c_int, [_vp]),
     "wise_device_status": (ctypes.c_int, [_vp]),
 }

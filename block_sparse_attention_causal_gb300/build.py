@@ -20,8 +20,9 @@ INCLUDE = os.path.join(REPO_DIR, "include")
 LIB_DIR = os.path.join(PKG_DIR, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libwise.so")
 
-SOURCES = ["wise_api.cu", "select_kernel.cu", "diag_kernel.cu", "attn_d64.cu", "attn_d96.cu", "attn_d128.cu"]
-HEADERS = ["ptx.cuh", "attn_kernel.cuh", "internal.h", "select_step.cuh", "select_keys.cuh"]
+SOURCES = ["wise_api.cu", "select_kernel.cu", "diag_kernel.cu", "gather_plan.cu", "attn_d64.cu", "attn_d96.cu",
+           "attn_d128.cu"]
+HEADERS = ["ptx.cuh", "attn_kernel.cuh", "internal.h", "select_step.cuh", "select_keys.cuh", "gather.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -41,6 +41,7 @@
 #pragma once
 #include <stdint.h>
 
+#include "gather.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "select_step.cuh"
@@ -379,42 +380,13 @@ static __device__ __forceinline__ void select_row_fused_any(const AttnParams& p,
 
 // ------------------------------------------------ gathered entries (B = 32)
 
-// Lane l's word of the key blocks listed by one CSR row (query block qb):
-// bit i is key block 32 l + i. [a, b) is the row's range in col_idx, v the
-// list's first 32 values (one per lane, INT32_MAX past b). Values outside
-// [0, qb] are skipped; they and values that do not ascend set `bad`.
-__device__ __forceinline__ uint32_t gather_list_bits(const AttnParams& p, int32_t a, int32_t b, int qb, int32_t v,
-                                                     int lane, bool& bad) {
-  uint32_t word = 0u;
-  int32_t prev = -1;
-  for (int32_t base = a; base < b; base += 32) {
-    if (base != a) v = (base + lane < b) ? __ldg(p.col_idx + base + lane) : INT32_MAX;
-    const bool in = base + lane < b;
-    int32_t pv = __shfl_up_sync(0xffffffffu, v, 1);
-    if (lane == 0) pv = prev;
-    const bool ok = in && v >= 0 && v > pv && v <= qb;
-    if (in && !ok) bad = true;
-    // OR each value's bit into the word of the lane that owns it, one
-    // target word per round
-    uint32_t pend = __ballot_sync(0xffffffffu, ok);
-    while (pend != 0u) {
-      const int tgt = __shfl_sync(0xffffffffu, v >> 5, __ffs(pend) - 1);
-      const bool mine = ok && (v >> 5) == tgt;
-      const uint32_t grp = __ballot_sync(0xffffffffu, mine);
-      const uint32_t bits = __reduce_or_sync(0xffffffffu, mine ? (1u << (v & 31)) : 0u);
-      if (lane == tgt) word |= bits;
-      pend &= ~grp;
-    }
-    prev = __shfl_sync(0xffffffffu, v, 31);
-  }
-  return word;
-}
-
 // The scheduler of sparse steps with blocks of 32, run by the whole warp.
-// A claimed unit's four CSR rows become per-lane bit words; each entry takes
-// the next four blocks of their union in ascending order, with the 4 x 4
-// mask of which query block lists which slot. Flow control and the order of
-// the two streams' records are those of the scheduler of the other variants.
+// With a plan (gather_plan.cu), a claimed unit's entries are read from it,
+// one per lane, 32 at a time. Without one, the unit's four CSR rows become
+// per-lane bit words and each entry takes the next four blocks of their
+// union in ascending order, with the 4 x 4 mask of which query block lists
+// which slot (gather.cuh). Flow control and the order of the two streams'
+// records are those of the scheduler of the other variants.
 template <class C>
 __device__ __forceinline__ void gather_scheduler(const AttnParams& p, const CUtensorMap* tm_q, GatherRec* meta,
                                                  uint32_t* qpos0, uint32_t* qpos1, volatile int* abort_flag,
@@ -465,7 +437,13 @@ __device__ __forceinline__ void gather_scheduler(const AttnParams& p, const CUte
     int unit, cnt;
     uint32_t kvrow0;  // first K/V row of the unit's key/value head
     bool alive;
+    // with a plan: the unit's entries (this lane holds entry 32 k + lane of
+    // the current group of 32) and their number
+    const uint32_t* pe;
+    int ne;
+    uint32_t e0, e1, e2;
   };
+  const bool planned = p.plan_counts != nullptr;
   GCur sc0, sc1;
   // a CTA's first two work-order positions are fixed (2b and 2b + 1); the
   // counter hands out the positions after the first 2 x gridDim
@@ -491,6 +469,29 @@ __device__ __forceinline__ void gather_scheduler(const AttnParams& p, const CUte
       const int bh = id / p.n_qtiles, t = id % p.n_qtiles;
       if (lane == 0)
         for (int c = 0; c < C::NCH; ++c) tma_prefetch_l2_2d(tm_q, c * C::CH, bh * p.n + t * 128);
+      sc.kvrow0 = (uint32_t)(((bh / p.heads) * (p.heads / p.kv_group) + (bh % p.heads) / p.kv_group) * p.n);
+      if (planned) {
+        // the unit's count and its first 32 entries, read together (tile t
+        // has room for t + 1 entries)
+        const uint32_t* pe = p.plan_entries + 4 * plan_entry_index(bh, t, p.n_qtiles);
+        const int ne = __ldg(p.plan_counts + id);
+        uint4 ev = make_uint4(0u, 0u, 0u, 0u);
+        if (lane <= t) ev = __ldg(reinterpret_cast<const uint4*>(pe) + lane);
+        if (ne <= 0 || ne > t + 1) {
+          if (ne != 0 && lane == 0) atomicOr(p.err, kErrBadSupport);
+          if (lane == 0) write_empty_unit(id, p, d);
+          __syncwarp();
+          continue;
+        }
+        sc.pe = pe;
+        sc.ne = ne;
+        sc.e0 = ev.x;
+        sc.e1 = ev.y;
+        sc.e2 = ev.z;
+        sc.unit = id;
+        sc.cnt = 0;
+        return true;
+      }
       // CSR rows of query blocks 4t .. 4t + nq - 1 (row_ptr entries 0 .. nq)
       const int qb0 = 4 * t;
       const int nq = min(4, p.nb - qb0);
@@ -510,10 +511,10 @@ __device__ __forceinline__ void gather_scheduler(const AttnParams& p, const CUte
         }
         v0[q] = (a[q] + lane < b[q]) ? __ldg(p.col_idx + a[q] + lane) : INT32_MAX;
       }
-      sc.w0 = gather_list_bits(p, a[0], b[0], qb0 + 0, v0[0], lane, bad);
-      sc.w1 = gather_list_bits(p, a[1], b[1], qb0 + 1, v0[1], lane, bad);
-      sc.w2 = gather_list_bits(p, a[2], b[2], qb0 + 2, v0[2], lane, bad);
-      sc.w3 = gather_list_bits(p, a[3], b[3], qb0 + 3, v0[3], lane, bad);
+      sc.w0 = gather_list_bits(p.col_idx, a[0], b[0], qb0 + 0, v0[0], lane, bad);
+      sc.w1 = gather_list_bits(p.col_idx, a[1], b[1], qb0 + 1, v0[1], lane, bad);
+      sc.w2 = gather_list_bits(p.col_idx, a[2], b[2], qb0 + 2, v0[2], lane, bad);
+      sc.w3 = gather_list_bits(p.col_idx, a[3], b[3], qb0 + 3, v0[3], lane, bad);
       sc.rem = sc.w0 | sc.w1 | sc.w2 | sc.w3;
       if (__any_sync(FULLM, bad) && lane == 0) atomicOr(p.err, kErrBadSupport);
       if (!__any_sync(FULLM, sc.rem != 0u)) {
@@ -523,37 +524,36 @@ __device__ __forceinline__ void gather_scheduler(const AttnParams& p, const CUte
       }
       sc.unit = id;
       sc.cnt = 0;
-      sc.kvrow0 = (uint32_t)(((bh / p.heads) * (p.heads / p.kv_group) + (bh % p.heads) / p.kv_group) * p.n);
       return true;
     }
   };
   // publish stream s's next entry; claim its next unit after the last one
   auto step = [&](GCur& sc, uint32_t sflag) -> bool {
-    uint32_t mask = 0u;
-    int kb[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t who = __ballot_sync(FULLM, sc.rem != 0u);
-      if (who == 0u) {
-        kb[c] = kb[c > 0 ? c - 1 : 0];  // nothing left: repeat the last block, masked
-      } else {
-        const int src = __ffs(who) - 1;
-        const int bit = (sc.rem != 0u) ? __ffs(sc.rem) - 1 : 0;
-        const uint32_t qm = ((sc.w0 >> bit) & 1u) | (((sc.w1 >> bit) & 1u) << 1) | (((sc.w2 >> bit) & 1u) << 2) |
-                            (((sc.w3 >> bit) & 1u) << 3);
-        if (lane == src) sc.rem &= sc.rem - 1u;
-        const int bsrc = __shfl_sync(FULLM, bit, src);
-        const uint32_t qsrc = __shfl_sync(FULLM, qm, src);
-        kb[c] = 32 * src + bsrc;
-        mask |= ((qsrc & 1u) << c) | (((qsrc >> 1) & 1u) << (4 + c)) | (((qsrc >> 2) & 1u) << (8 + c)) |
-                (((qsrc >> 3) & 1u) << (12 + c));
+    uint32_t mask, kb01, kb23;
+    bool more;
+    if (planned) {
+      const int c = sc.cnt;
+      if (c > 0 && (c & 31) == 0) {
+        // the next 32 of a long tile's entries
+        uint4 ev = make_uint4(0u, 0u, 0u, 0u);
+        if (c + lane < sc.ne) ev = __ldg(reinterpret_cast<const uint4*>(sc.pe) + c + lane);
+        sc.e0 = ev.x;
+        sc.e1 = ev.y;
+        sc.e2 = ev.z;
       }
+      kb01 = __shfl_sync(FULLM, sc.e0, c & 31);
+      kb23 = __shfl_sync(FULLM, sc.e1, c & 31);
+      mask = __shfl_sync(FULLM, sc.e2, c & 31) & 0xffffu;
+      more = c + 1 < sc.ne;
+    } else {
+      int kb[4] = {0, 0, 0, 0};
+      mask = gather_take_entry(sc.rem, sc.w0, sc.w1, sc.w2, sc.w3, lane, kb);
+      kb01 = (uint32_t)kb[0] | ((uint32_t)kb[1] << 16);
+      kb23 = (uint32_t)kb[2] | ((uint32_t)kb[3] << 16);
+      more = __any_sync(FULLM, sc.rem != 0u);
     }
-    const bool more = __any_sync(FULLM, sc.rem != 0u);
     const uint32_t info = (sc.cnt == 0 ? kEntFirst : 0u) | (more ? 0u : kEntLast) | sflag | (mask << 8);
-    if (!publish(info, (uint32_t)kb[0] | ((uint32_t)kb[1] << 16), (uint32_t)sc.unit,
-                 (uint32_t)kb[2] | ((uint32_t)kb[3] << 16), sc.kvrow0))
-      return false;
+    if (!publish(info, kb01, (uint32_t)sc.unit, kb23, sc.kvrow0)) return false;
     ++sc.cnt;
     if (more) return true;
     sc.alive = claim(sc);

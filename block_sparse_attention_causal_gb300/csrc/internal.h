@@ -37,7 +37,37 @@ struct AttnParams {
   int32_t sel_nwords;
   int32_t sel_first, sel_last;
   uint32_t sel_flags;
+  // Sparse steps with blocks of 32: the tiles' gathered entries, built once
+  // per support (gather_plan.cu). Without them (null) the scheduler forms
+  // each claimed tile's entries from its four CSR rows.
+  const int32_t* plan_counts;    // [n_units] entries per tile
+  const uint32_t* plan_entries;  // 4 words per entry, at plan_entry_index(bh, t, n_qtiles)
 };
+
+// Gathered-entry plan of sparse steps with blocks of 32: per work unit (one
+// 128-row tile of one (batch, head) slice) its entry count, then, 16-byte
+// aligned, the entries of each slice as a triangle: tile t has at most t + 1
+// (its query blocks admit key blocks 0 .. 4t + 3, four per entry). An entry
+// is four words: key blocks of slots 0 | 1 << 16, of slots 2 | 3 << 16, the
+// slot mask (bit 4j + c: query block j of the tile lists slot c's block), 0.
+__host__ __device__ inline int64_t plan_entry_index(int64_t bh, int64_t t, int64_t n_qtiles) {
+  return bh * (n_qtiles * (n_qtiles + 1) / 2) + t * (t + 1) / 2;
+}
+__host__ __device__ inline int64_t plan_counts_bytes(int64_t n_units) { return (n_units * 4 + 15) / 16 * 16; }
+__host__ __device__ inline int64_t plan_bytes(int64_t bh, int64_t n_qtiles) {
+  return plan_counts_bytes(bh * n_qtiles) + plan_entry_index(bh, 0, n_qtiles) * 16;
+}
+
+struct GatherPlanLaunch {
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  int64_t col_cap;
+  int32_t bh_count, nb, n_qtiles;
+  int32_t* counts;
+  uint32_t* entries;
+  uint32_t* err;
+};
+cudaError_t launch_gather_plan(const GatherPlanLaunch& g, cudaStream_t stream);
 
 struct SelectLaunch {
   const float* mass;

@@ -141,7 +141,7 @@ struct FusedSelect {
 int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, const void* v, void* o, float* lse,
                      float* mass, void* ws, const int32_t* row_ptr, const int32_t* col_idx, int64_t col_cap,
                      const int32_t* tile_order, bool sparse, cudaStream_t stream,
-                     const FusedSelect* fs = nullptr) {
+                     const FusedSelect* fs = nullptr, const void* plan = nullptr) {
   const Shape s = shape_of(desc);
   uint32_t* err = error_word();
   if (!err) return WISE_ERR_CUDA;
@@ -181,6 +181,11 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
   p.tile_order = tile_order;
   p.n_units = s.n_units;
   p.err = err;
+  if (plan) {
+    p.plan_counts = static_cast<const int32_t*>(plan);
+    p.plan_entries = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(plan) +
+                                                        plan_counts_bytes(s.n_units));
+  }
   if (fs) {
     p.sel_bits = fs->bits;
     p.sel_counts = fs->counts;
@@ -317,6 +322,55 @@ int wise_attn_sparse(const wise_attn_desc* desc, const void* q, const void* k, c
     return WISE_ERR_ALIGNMENT;
   return launch_attention(desc, q, k, v, o, lse, nullptr, nullptr, row_ptr, col_idx, col_capacity, tile_order, true,
                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+int wise_attn_sparse_planned(const wise_attn_desc* desc, const void* q, const void* k, const void* v,
+                             const int32_t* row_ptr, const int32_t* col_idx, int64_t col_capacity,
+                             const int32_t* tile_order, const void* plan, void* o, float* lse,
+                             wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (!q || !k || !v || !o || !row_ptr || !col_idx || col_capacity < 0) return WISE_ERR_INVALID_ARGUMENT;
+  if (plan && desc->block != 32) return WISE_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (plan && !aligned16(plan)))
+    return WISE_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(row_ptr) & 3u) || (reinterpret_cast<uintptr_t>(col_idx) & 3u) ||
+      (tile_order && (reinterpret_cast<uintptr_t>(tile_order) & 3u)) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return WISE_ERR_ALIGNMENT;
+  return launch_attention(desc, q, k, v, o, lse, nullptr, nullptr, row_ptr, col_idx, col_capacity, tile_order, true,
+                          reinterpret_cast<cudaStream_t>(stream), nullptr, plan);
+}
+
+size_t wise_gather_plan_bytes(const wise_attn_desc* desc) {
+  if (check_desc(desc) != WISE_OK || desc->block != 32) return 0;
+  const Shape s = shape_of(desc);
+  return (size_t)plan_bytes(s.bh, s.n_qtiles);
+}
+
+int wise_gather_plan(const wise_attn_desc* desc, const int32_t* row_ptr, const int32_t* col_idx,
+                     int64_t col_capacity, void* plan, size_t plan_bytes_given, wise_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != WISE_OK) return st;
+  if (desc->block != 32) return WISE_ERR_UNSUPPORTED;
+  if (!row_ptr || !col_idx || !plan || col_capacity < 0) return WISE_ERR_INVALID_ARGUMENT;
+  if (plan_bytes_given < wise_gather_plan_bytes(desc)) return WISE_ERR_WORKSPACE;
+  if (!aligned16(plan) || (reinterpret_cast<uintptr_t>(row_ptr) & 3u) || (reinterpret_cast<uintptr_t>(col_idx) & 3u))
+    return WISE_ERR_ALIGNMENT;
+  uint32_t* err = error_word();
+  if (!err) return WISE_ERR_CUDA;
+  const Shape s = shape_of(desc);
+  GatherPlanLaunch g;
+  g.row_ptr = row_ptr;
+  g.col_idx = col_idx;
+  g.col_cap = col_capacity;
+  g.bh_count = (int32_t)s.bh;
+  g.nb = s.nb;
+  g.n_qtiles = s.n_qtiles;
+  g.counts = static_cast<int32_t*>(plan);
+  g.entries = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(plan) + plan_counts_bytes(s.n_units));
+  g.err = err;
+  return launch_gather_plan(g, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? WISE_OK : WISE_ERR_CUDA;
 }
 
 int wise_select_support(const wise_attn_desc* desc, const float* block_mass, int32_t window, double eta,

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define WISE_ABI_VERSION 4
+#define WISE_ABI_VERSION 5
 
 typedef struct CUstream_st* wise_stream_t; /* same type as cudaStream_t */
 
@@ -263,6 +263,47 @@ int wise_select_support_noalloc(const wise_attn_desc* desc, const float* block_m
 int wise_attn_sparse(const wise_attn_desc* desc, const void* q, const void* k, const void* v,
                      const int32_t* row_ptr, const int32_t* col_idx, int64_t col_capacity,
                      const int32_t* tile_order, void* o, float* lse, wise_stream_t stream);
+
+/*
+ * wise_gather_plan_bytes / wise_gather_plan -- for blocks of 32 only: the
+ * late steps' gathered entries of every 128-row tile, built once from the
+ * support CSR and reused by every late step (WISE Appendix B
+ * "Sparse-kernel implementation": the schedule is built once after
+ * discovery). A tile holds four 32-row query blocks; an entry is the next
+ * four key blocks of the union of their lists, in ascending order, with
+ * the mask of which query block lists which of the four. Without a plan,
+ * wise_attn_sparse forms the same entries from the CSR on every late step.
+ *   wise_gather_plan_bytes : bytes of the plan for desc (0 unless
+ *                desc->block == 32): an int32 count per tile, then, 16-byte
+ *                aligned, 16 bytes per entry, tile t of each (batch, head)
+ *                slice owning room for t + 1 entries.
+ *   row_ptr, col_idx, col_capacity : the support CSR (device), as for
+ *                wise_attn_sparse; entries breaking its rules are skipped
+ *                and flagged (WISE_ERR_BAD_SUPPORT in the device word).
+ *   plan, plan_bytes : device buffer (caller-owned, 16-byte aligned), at
+ *                least wise_gather_plan_bytes(desc). Every tile's count and
+ *                entries are written; it stays valid while the CSR is not
+ *                changed.
+ * Returns WISE_ERR_UNSUPPORTED for other block sizes, WISE_ERR_WORKSPACE if
+ * plan_bytes is too small. One launch on `stream`.
+ */
+size_t wise_gather_plan_bytes(const wise_attn_desc* desc);
+int wise_gather_plan(const wise_attn_desc* desc, const int32_t* row_ptr, const int32_t* col_idx,
+                     int64_t col_capacity, void* plan, size_t plan_bytes, wise_stream_t stream);
+
+/*
+ * wise_attn_sparse_planned -- wise_attn_sparse (§5.2 Eq 8) over a support
+ * whose gathered entries were built by wise_gather_plan from the same CSR
+ * (blocks of 32; plan NULL = wise_attn_sparse). The results are the same bits
+ * as without the plan: the entries, their order and the arithmetic are the
+ * same; the late step only reads them instead of forming them. A plan whose
+ * counts exceed a tile's room is flagged (WISE_ERR_BAD_SUPPORT) and its tile
+ * is written as empty.
+ */
+int wise_attn_sparse_planned(const wise_attn_desc* desc, const void* q, const void* k, const void* v,
+                             const int32_t* row_ptr, const int32_t* col_idx, int64_t col_capacity,
+                             const int32_t* tile_order, const void* plan, void* o, float* lse,
+                             wise_stream_t stream);
 
 /*
  * wise_select_control -- the early-static support controls of WISE Appendix B

@@ -137,6 +137,31 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.wise_attn_sparse(d, 16, 16, 16, None, 16, 10, None, 16, None, None) == _lib.WISE_ERR_INVALID_ARGUMENT
 
 
+def test_gather_plan_argument_checks(lib):
+    """The plan of gathered entries exists for blocks of 32 only: its size
+    (an int32 count per 128-row tile, 16-byte aligned, then 16 bytes per
+    entry, tile t of each slice owning room for t + 1) and the argument
+    checks of building and using it (no device work)."""
+    d64 = _desc()
+    d32 = _lib.make_desc(2, 3, 1024, 64, 32)
+    assert lib.wise_gather_plan_bytes(d64) == 0
+    tiles, units = 8, 2 * 3 * 8
+    assert lib.wise_gather_plan_bytes(d32) == (units * 4 + 15) // 16 * 16 + 2 * 3 * (tiles * (tiles + 1) // 2) * 16
+    nbytes = lib.wise_gather_plan_bytes(d32)
+    assert lib.wise_gather_plan(d64, 16, 16, 10, 16, 1 << 20, None) == _lib.WISE_ERR_UNSUPPORTED
+    assert lib.wise_gather_plan(d32, None, 16, 10, 16, nbytes, None) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert lib.wise_gather_plan(d32, 16, 16, 10, None, nbytes, None) == _lib.WISE_ERR_INVALID_ARGUMENT
+    assert lib.wise_gather_plan(d32, 16, 16, 10, 16, nbytes - 1, None) == _lib.WISE_ERR_WORKSPACE
+    assert lib.wise_gather_plan(d32, 16, 16, 10, 8, nbytes, None) == _lib.WISE_ERR_ALIGNMENT
+    # a plan with another block size, and the usual checks of the sparse step
+    assert lib.wise_attn_sparse_planned(d64, 16, 16, 16, 16, 16, 10, None, 16, 16, None, None) == \
+        _lib.WISE_ERR_INVALID_ARGUMENT
+    assert lib.wise_attn_sparse_planned(d32, 16, 16, 16, None, 16, 10, None, 16, 16, None, None) == \
+        _lib.WISE_ERR_INVALID_ARGUMENT
+    assert lib.wise_attn_sparse_planned(d32, 16, 16, 16, 16, 16, 10, None, 8, 16, None, None) == \
+        _lib.WISE_ERR_ALIGNMENT
+
+
 def test_select_argument_checks(lib):
     d = _desc()
     cap = lib.wise_support_capacity(d)

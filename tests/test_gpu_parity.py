@@ -732,7 +732,42 @@ def _sparse_vs_oracle(x, q, k, v, rows, b, h, n, d, blk=32, use_schedule=False):
     o_ref, lse_ref = O.sparse(x[0].astype(np.float64), x[1].astype(np.float64), x[2].astype(np.float64), blk, rp, ci)
     _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
     _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+    if blk == 32:
+        # the same step over the tiles' gathered entries read from a plan:
+        # the same entries in the same order, so the same bits
+        wise.gather_plan(sup)
+        o_p, lse_p = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=use_schedule)
+        wise.check_device()
+        assert torch.equal(o_p, o) and torch.equal(lse_p, lse)
+        _check_plan(sup, rows)
     return o, lse
+
+
+def _check_plan(sup, rows):
+    """The plan's counts and entries against their definition: per 128-row
+    tile, the union of its four query blocks' lists in ascending order, four
+    key blocks per entry (the last repeated to fill the entry), with bit
+    4j + c set when query block j lists slot c's block."""
+    b, h, nb = sup.batch, sup.heads, sup.n_blocks
+    tiles = (nb + 3) // 4
+    raw = sup.plan.cpu().numpy()
+    units = b * h * tiles
+    counts = raw[:units * 4].view(np.int32)
+    off = (units * 4 + 15) // 16 * 16
+    words = raw[off:].view(np.uint32)
+    for bh in range(b * h):
+        for t in range(tiles):
+            lists = [set(rows[bh * nb + qb]) for qb in range(4 * t, min(4 * t + 4, nb))]
+            union = sorted(set().union(*lists))
+            chunks = [union[i:i + 4] for i in range(0, len(union), 4)]
+            u = bh * tiles + t
+            assert counts[u] == len(chunks), (bh, t)
+            base = bh * (tiles * (tiles + 1) // 2) + t * (t + 1) // 2
+            for e, ch in enumerate(chunks):
+                kb = ch + [ch[-1]] * (4 - len(ch))
+                mask = sum(1 << (4 * j + c) for j, lst in enumerate(lists) for c in range(len(ch)) if ch[c] in lst)
+                w = words[4 * (base + e):4 * (base + e) + 3]
+                assert (int(w[0]), int(w[1]), int(w[2])) == (kb[0] | kb[1] << 16, kb[2] | kb[3] << 16, mask), (bh, t, e)
 
 
 @pytest.mark.parametrize("shape", B32_SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -846,6 +881,9 @@ def test_block32_trajectory_end_to_end():
             _assert_support_matches(rows[base:base + nb], om, cfg, rows[base:base + nb])
     rp = sup.row_ptr.cpu().numpy()
     ci = sup.col_idx.cpu().numpy()
+    # the selection built the late steps' plan of gathered entries
+    assert sup.plan is not None
+    _check_plan(sup, rows)
     for t in range(cfg.t_d, cfg.steps):
         x = wl.step_inputs(cfg, t)
         q, k, v = (torch.from_numpy(x[i]).to(torch.bfloat16).cuda() for i in range(3))
@@ -854,6 +892,8 @@ def test_block32_trajectory_end_to_end():
                                   cfg.block, rp, ci)
         _assert_close("O", o.cpu().numpy(), o_ref, O_TOL)
         _assert_close("LSE", lse.cpu().numpy(), lse_ref, LSE_TOL)
+        o_u, lse_u = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_plan=False)
+        assert torch.equal(o_u, o) and torch.equal(lse_u, lse)
 
 
 # ------------------- selection fused into discovery (Eq 6 streamed over the window) ----

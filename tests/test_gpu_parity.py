@@ -830,6 +830,19 @@ def test_block32_sparse_malformed_support_is_flagged_not_faulted():
     wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
     assert wise.device_status() == wise._lib.WISE_ERR_BAD_SUPPORT
     assert wise.device_status() == wise._lib.WISE_OK
+    # the plan built from it skips and flags the same entries; the step over
+    # the plan then reads only what the plan holds
+    wise.gather_plan(sup)
+    assert wise.device_status() == wise._lib.WISE_ERR_BAD_SUPPORT
+    wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    assert wise.device_status() == wise._lib.WISE_OK
+    # a plan whose count exceeds a tile's room (t + 1 entries) is flagged and
+    # its tile written as empty
+    counts = sup.plan[:8].view(torch.int32)
+    counts[1] = 9
+    o, lse = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    assert wise.device_status() == wise._lib.WISE_ERR_BAD_SUPPORT
+    assert torch.all(o[0, 0, 128:256] == 0) and torch.all(torch.isneginf(lse[0, 0, 128:256]))
 
 
 @pytest.mark.parametrize("case", [(2, 1, 2, 40, 0.9), (3, 2, 1, 128, 0.95), (1, 1, 1, 1024, 0.8), (2, 1, 3, 7, 0.9)],

@@ -451,7 +451,7 @@ def run_gpu(args, rank, world):
                 elif t == td - 1:
                     timer("select", lambda: wise.select_support(masses, n, d, blk, cfg.eta, support=support,
                                                                 workspace=sel_ws), record)
-                    launches += 2
+                    launches += 3 if blk == 32 else 2  # Eq 6, finalize (+ the plan of gathered entries)
             else:
                 timer("sparse", lambda: wise.sparse(q, k, v, support, out=o, lse=lse), record)
                 launches += 1
@@ -492,6 +492,29 @@ def run_gpu(args, rank, world):
     sparse_tile_flops = tile_flops(entries, blk, d)
     dense_flops = wise.dense_flops(B, H, n, d)
     density = float(rp[-1]) / (B * H * nb * (nb + 1) / 2)
+
+    # ------------------------------------------------------------ the same trajectory as one CUDA graph
+    # (captured once, replayed: no host launch gaps between its launches)
+    graph_ms = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            trajectory(dev_in)
+        graph.replay()
+        barrier()
+        wise.check_device()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        barrier()
+        wise.check_device()
+        graph_ms = g0.elapsed_time(g1) / args.steps
+        del graph
+    except RuntimeError as e:  # capture refused: report it, keep the eager numbers
+        graph_ms = f"capture failed: {e}"[:160]
 
     # ------------------------------------------------------------ the library's dense kernel, same late inputs
     dtimer = Timer(stream)
@@ -599,6 +622,8 @@ def run_gpu(args, rank, world):
                            "dense_step": round(dense_ms, 4), "window": W},
         "setup_inclusive_speedup": round((n_late * dense_ms) / (setup_ms + n_late * sparse_ms), 3),
         "trajectory_speedup": round(T * dense_ms / traj_ms, 3),
+        # the same trajectory captured once as a CUDA graph and replayed
+        "trajectory_graph_ms": round(graph_ms, 4) if isinstance(graph_ms, float) else graph_ms,
         "kernels": {k_: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in s.items()}
                     for k_, s in kern_stats.items()},
         "roofline": roofline, "roofline_sparse": sparse_roof,

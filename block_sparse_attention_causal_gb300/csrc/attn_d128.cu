@@ -1,6 +1,4 @@
 // Instantiations of the tcgen05 attention kernel for head_dim = 128.
-#include <atomic>
-
 #include "attn_kernel.cuh"
 
 namespace wise {
@@ -23,11 +21,14 @@ cudaError_t launch_one(const CUtensorMap* m, const AttnParams& p, cudaStream_t s
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  // persistent: one CTA per SM (the shared-memory footprint allows no more);
-  // each launch takes the next work-counter slot
-  static std::atomic<uint32_t> launches{0};
+  // persistent: one CTA per SM (the shared-memory footprint allows no more).
+  // p.sched_slot is the launch's ticket (launch_attention): eager launches
+  // take the lower half of the work-counter slots, launches recorded into a
+  // CUDA graph the upper half, so a graph's replay never shares a slot with
+  // an eager launch running beside it
   AttnParams q = p;
-  q.sched_slot = launches.fetch_add(1u) % kSchedSlots;
+  constexpr uint32_t half = kSchedSlots / 2;
+  q.sched_slot = (p.sched_slot >> 31) ? half + (p.sched_slot & 0x7fffffffu) % half : p.sched_slot % half;
   const int64_t grid = p.n_units < sm_count[dev] ? p.n_units : sm_count[dev];
   wise_attn_kernel<D, BN, SPARSE><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(m[0], m[1], m[2], m[3], m[4], q);
   return cudaGetLastError();

@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -196,6 +197,14 @@ int launch_attention(const wise_attn_desc* desc, const void* q, const void* k, c
     p.sel_last = fs->last;
     p.sel_flags = fs->flags;
   }
+  // The launch's work-counter ticket, one sequence shared by every attention
+  // kernel (launches on different streams may run at the same time, so each
+  // must hold its own slot); bit 31 marks a launch recorded into a CUDA graph
+  static std::atomic<uint32_t> eager_tickets{0}, graph_tickets{0};
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return WISE_ERR_CUDA;
+  p.sched_slot = (cap == cudaStreamCaptureStatusActive) ? (0x80000000u | (graph_tickets.fetch_add(1u) & 0x7fffffffu))
+                                                        : (eager_tickets.fetch_add(1u) & 0x7fffffffu);
   cudaError_t e;
   switch (s.d) {
     case 64: e = launch_attn_d64(s.bn, sparse, maps, p, stream); break;

@@ -48,6 +48,11 @@
  *   leaves its counter at zero when it ends), and the scratch array of
  *   wise_select_support_noalloc. Calls are asynchronous and ordered on the
  *   given stream (a cudaStream_t; NULL means the legacy default stream).
+ * - Calls may be recorded into a CUDA graph (stream capture) and replayed.
+ *   The attention kernels each hold a work-counter slot for the length of a
+ *   launch; eager launches and recorded ones draw from separate halves of the
+ *   slots, so replays and eager calls on other streams can run side by side.
+ *   One graph must not be replayed on two streams at once.
  * - Argument, shape and alignment errors are reported before any launch and
  *   nothing is written. A failed launch returns WISE_ERR_CUDA. Kernel-side
  *   problems (a malformed support list, a wait that timed out) are recorded in

@@ -3,25 +3,29 @@
 // (WISE) plus the CSR schedule of its Appendix B "Sparse-kernel
 // implementation".
 //
-//  select_rows_kernel : one warp per (batch, head, query block) row. For each
-//      window step it finds the Eq 6 support without sorting (select_step.cuh:
-//      int64 fixed point, a search for the k-th mass, near-ties toward lower
-//      indices). Element jj of lane l is block 32*jj + l, so the ballot at
-//      step jj is word jj of the row's support bitmask (kept by lane jj).
-//      Steps are OR-ed, then the sink / diagonal blocks added.
-//      The same kernel builds the two early-static controls of WISE's
-//      Appendix B ("Intervention controls") from one step's masses and a
-//      reference working set: MassMatched (Eqs 20-21) replaces eta by the
-//      row's mass covered by the reference, summed in the same fixed point;
-//      SizeMatched (Eq 22) keeps the reference's block count k and finds the
-//      k-th mass with a bitwise search on counts instead of sums.
-//  finalize_kernel    : row_ptr (each chunk of rows takes the count of the
-//      rows before it from the chunks before it, by a decoupled look-back),
-//      nnz, ascending col_idx from the bitmasks, and the late-step work order:
-//      every unit of the launch sorted by number of listed blocks, heaviest
-//      first (ties by unit index), so that no heavy unit starts near the end
-//      of a sparse step. Shapes whose ranking does not fit in one CTA's
-//      shared memory are ranked per group of (batch, head) slices.
+//  select_steps_kernel : Eq 6, one warp per (row, window step) with the row's
+//      window warps in one CTA. The row's masses (lane l holds blocks
+//      32*jj + l) are cut at the k-th mass on their float keys where the
+//      2^-52 fixed point is exact (select_keys.cuh), else in the fixed point
+//      (select_step.cuh); near-ties go toward lower indices. The ballot at
+//      round jj is word jj of the step support (kept by lane jj); the steps
+//      are OR-ed in shared memory, then the sink / diagonal blocks added.
+//      CTAs run the query blocks from the last down (longest rows first).
+//  select_rows_kernel  : the two early-static controls of WISE's Appendix B
+//      ("Intervention controls") from one step's masses and a reference
+//      working set, one warp per row: MassMatched (Eqs 20-21) replaces eta
+//      by the row's mass covered by the reference, summed in the same fixed
+//      point; SizeMatched (Eq 22) keeps the reference's block count k and
+//      finds the k-th mass with a bitwise search on counts instead of sums.
+//  finalize_kernel     : a dependent launch after either. row_ptr (a chunk
+//      of rows sums the counts of all earlier rows from one bulk copy when it
+//      starts early in the rows, else takes them from the chunks before it by
+//      a decoupled look-back), nnz, ascending col_idx from the bitmasks, and
+//      the late-step work order: every unit of the launch sorted by number of
+//      listed blocks, heaviest first (ties by unit index), so that no heavy
+//      unit starts near the end of a sparse step. Shapes whose ranking does
+//      not fit in one CTA's shared memory are ranked per group of (batch,
+//      head) slices.
 #include <stdint.h>
 
 #include "internal.h"

@@ -809,6 +809,27 @@ def test_block32_sparse_full_support_bitwise_equals_discover():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_block32_planned_long_tiles_bitwise_equals_discover():
+    """Tiles with more than 32 gathered entries (the late step reads a long
+    tile's plan entries 32 at a time): the full causal support at 8K (tile t
+    holds t + 1 entries, up to 64) over the plan equals discovery bit for bit,
+    and so does the same step without the plan."""
+    b, h, n, d = 1, 1, 8192, 64
+    x, q, k, v = _bf16_inputs(b, h, n, d, seed=29, scale=1.5, planted=2)
+    nb = n // 32
+    rows = [list(range(qb + 1)) for qb in range(nb)]
+    sup = wise.support_from_lists(rows, b, h, n, d, 32)
+    wise.gather_plan(sup)
+    counts = sup.plan[:4 * (nb // 4)].view(torch.int32).cpu().numpy()
+    assert counts.max() == nb // 4 and np.array_equal(counts, np.arange(1, nb // 4 + 1))
+    o1, l1 = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False)
+    o2, l2 = wise.sparse(q, k, v, sup, out_dtype=torch.float32, use_schedule=False, use_plan=False)
+    o3, l3, _ = wise.discover(q, k, v, 32, want_mass=False, out_dtype=torch.float32)
+    wise.check_device()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
 def test_block32_sparse_empty_rows_and_tiles():
     b, h, n, d = 1, 1, 512, 64
     x, q, k, v = _bf16_inputs(b, h, n, d, seed=6)

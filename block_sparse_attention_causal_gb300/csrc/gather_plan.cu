@@ -4,11 +4,11 @@
 // "Sparse-kernel implementation": the schedule is built once after discovery
 // and reused by every late step). One warp per 128-row tile: the union of its
 // four query blocks' lists in ascending order, four key blocks per entry,
-// with the mask of which query block lists which slot (gather.cuh) -- the
-// entries the late-step scheduler would otherwise form on every claim.
+// with the mask of which query block lists which slot -- the entries that
+// the late-step scheduler would otherwise form one at a time on every claim
+// (gather.cuh).
 #include <stdint.h>
 
-#include "gather.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
